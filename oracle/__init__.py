@@ -1,0 +1,257 @@
+"""NVFP4 oracle (test infrastructure only).
+
+A plain CPU statement of the NVFP4 path, in C (nvfp4_oracle.c: float64 and
+exact 128-bit integer arithmetic, float32 only where the quantisation recipe
+fixes float32), wrapped here with ctypes and numpy. Only tests/,
+__graft_entry__.smoke() and bench.py's CPU-baseline leg use it; the library
+never does, and the two share no code.
+
+What is computed, and from which passage, is stated in nvfp4_oracle.c's header.
+Every function here is pinned by a CPU test against something other than
+itself (format tables, brute-force enumeration, exact integer arithmetic,
+library routines, closed forms); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nvfp4_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libnvfp4_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_u64p = ctypes.POINTER(ctypes.c_uint64)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_f64p = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP if available). Returns the .so path."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    base = ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-shared",
+            "-fPIC", "-o", _LIB_PATH + ".tmp", _SRC, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_LIB_PATH + ".tmp", _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            L.nvo_e2m1_value.restype = ctypes.c_double
+            L.nvo_e2m1_value.argtypes = [ctypes.c_int]
+            L.nvo_e4m3_value.restype = ctypes.c_double
+            L.nvo_e4m3_value.argtypes = [ctypes.c_int]
+            L.nvo_e2m1_encode.restype = ctypes.c_int
+            L.nvo_e2m1_encode.argtypes = [ctypes.c_float]
+            L.nvo_e4m3_encode.restype = ctypes.c_int
+            L.nvo_e4m3_encode.argtypes = [ctypes.c_float]
+            L.nvo_e2m1_encode_n.argtypes = [_f32p, ctypes.c_int64, _u8p]
+            L.nvo_e4m3_encode_n.argtypes = [_f32p, ctypes.c_int64, _u8p]
+            L.nvo_scale_bytes.restype = ctypes.c_int64
+            L.nvo_scale_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+            L.nvo_sf_offset.restype = ctypes.c_int64
+            L.nvo_sf_offset.argtypes = [ctypes.c_int64] * 3
+            L.nvo_sf_unswizzle.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p]
+            L.nvo_sf_swizzle.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p]
+            L.nvo_amax_bf16.restype = ctypes.c_float
+            L.nvo_amax_bf16.argtypes = [_u16p, ctypes.c_int64]
+            L.nvo_global_scale.restype = ctypes.c_float
+            L.nvo_global_scale.argtypes = [ctypes.c_float]
+            L.nvo_quantize.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
+                                       _u8p, _u8p]
+            L.nvo_dequantize.argtypes = [_u8p, _u8p, ctypes.c_float, ctypes.c_int64,
+                                         ctypes.c_int64, _f64p]
+            L.nvo_gemm_f64.argtypes = [_u8p, _u8p, ctypes.c_float, _u8p, _u8p, ctypes.c_float,
+                                       ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                       _i64p, ctypes.c_int64, _i64p, ctypes.c_int64,
+                                       _f64p, _f64p]
+            L.nvo_gemm_exact.restype = ctypes.c_int
+            L.nvo_gemm_exact.argtypes = [_u8p, _u8p, _u8p, _u8p, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_int64, _i64p, _u64p]
+            L.nvo_grouped_gemm_f64.restype = ctypes.c_int
+            L.nvo_grouped_gemm_f64.argtypes = [_u8p, _u8p, ctypes.c_float, _u8p, _u8p, _f32p,
+                                               _i32p, ctypes.c_int32, ctypes.c_int64,
+                                               ctypes.c_int64, ctypes.c_int64, _i64p,
+                                               ctypes.c_int64, _i64p, ctypes.c_int64,
+                                               _f64p, _f64p]
+            L.nvo_num_threads.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray, t):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(t)
+
+
+def _opt_idx(idx):
+    if idx is None:
+        return None, 0, None
+    arr = np.ascontiguousarray(idx, dtype=np.int64)
+    return arr, len(arr), _p(arr, _i64p)
+
+
+# ---- formats -----------------------------------------------------------------
+
+def e2m1_value(code: int) -> float:
+    return lib().nvo_e2m1_value(int(code))
+
+
+def e4m3_value(code: int) -> float:
+    return lib().nvo_e4m3_value(int(code))
+
+
+def e2m1_encode(v: float) -> int:
+    return lib().nvo_e2m1_encode(float(v))
+
+
+def e4m3_encode(t: float) -> int:
+    return lib().nvo_e4m3_encode(float(t))
+
+
+def e2m1_encode_array(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.zeros(v.shape, dtype=np.uint8)
+    lib().nvo_e2m1_encode_n(_p(v, _f32p), v.size, _p(out, _u8p))
+    return out
+
+
+def e4m3_encode_array(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.zeros(v.shape, dtype=np.uint8)
+    lib().nvo_e4m3_encode_n(_p(v, _f32p), v.size, _p(out, _u8p))
+    return out
+
+
+def scale_bytes(rows: int, K: int) -> int:
+    return int(lib().nvo_scale_bytes(rows, K))
+
+
+def sf_offset(r: int, c: int, K: int) -> int:
+    return int(lib().nvo_sf_offset(r, c, K))
+
+
+def sf_unswizzle(sf: np.ndarray, rows: int, K: int) -> np.ndarray:
+    lin = np.zeros((rows, K // 16), dtype=np.uint8)
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    lib().nvo_sf_unswizzle(_p(sf, _u8p), rows, K, _p(lin, _u8p))
+    return lin
+
+
+def sf_swizzle(lin: np.ndarray, rows: int, K: int) -> np.ndarray:
+    sf = np.zeros(scale_bytes(rows, K), dtype=np.uint8)
+    lin = np.ascontiguousarray(lin, dtype=np.uint8)
+    lib().nvo_sf_swizzle(_p(lin, _u8p), rows, K, _p(sf, _u8p))
+    return sf
+
+
+# ---- quantisation --------------------------------------------------------------
+
+def amax(x_bf16: np.ndarray) -> float:
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    return float(np.float32(lib().nvo_amax_bf16(_p(x, _u16p), x.size)))
+
+
+def global_scale(amax_value: float) -> np.float32:
+    return np.float32(lib().nvo_global_scale(float(amax_value)))
+
+
+def quantize(x_bf16: np.ndarray, g=None):
+    """bf16 bits [M, K] -> (q [M, K/2] u8, sf swizzled u8, g float32)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M, K = x.shape
+    if g is None:
+        g = global_scale(amax(x))
+    q = np.zeros((M, K // 2), dtype=np.uint8)
+    sf = np.zeros(scale_bytes(M, K), dtype=np.uint8)
+    lib().nvo_quantize(_p(x, _u16p), M, K, float(g), _p(q, _u8p), _p(sf, _u8p))
+    return q, sf, np.float32(g)
+
+
+def dequantize(q: np.ndarray, sf: np.ndarray, g: float, rows: int, K: int) -> np.ndarray:
+    out = np.zeros((rows, K), dtype=np.float64)
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    lib().nvo_dequantize(_p(q, _u8p), _p(sf, _u8p), float(g), rows, K, _p(out, _f64p))
+    return out
+
+
+# ---- GEMM ------------------------------------------------------------------------
+
+def gemm(a, sfa, ga, b, sfb, gb, M, N, K, rows=None, cols=None):
+    """float64 y [nr, nc] and the tolerance magnitude term sum_k |x^ w^| (same shape)."""
+    a, sfa, b, sfb = (np.ascontiguousarray(t, dtype=np.uint8) for t in (a, sfa, b, sfb))
+    r_arr, nr, r_ptr = _opt_idx(rows)
+    c_arr, nc, c_ptr = _opt_idx(cols)
+    nr = M if rows is None else nr
+    nc = N if cols is None else nc
+    y = np.zeros((nr, nc), dtype=np.float64)
+    ad = np.zeros((nr, nc), dtype=np.float64)
+    lib().nvo_gemm_f64(_p(a, _u8p), _p(sfa, _u8p), float(ga), _p(b, _u8p), _p(sfb, _u8p),
+                       float(gb), M, N, K, r_ptr, nr, c_ptr, nc, _p(y, _f64p), _p(ad, _f64p))
+    return y, ad
+
+
+def gemm_exact(a, sfa, b, sfb, M, N, K):
+    """Exact integer sums S [M, N] (Python ints); the real dot product is S * 2^-20."""
+    a, sfa, b, sfb = (np.ascontiguousarray(t, dtype=np.uint8) for t in (a, sfa, b, sfb))
+    hi = np.zeros((M, N), dtype=np.int64)
+    lo = np.zeros((M, N), dtype=np.uint64)
+    nan = lib().nvo_gemm_exact(_p(a, _u8p), _p(sfa, _u8p), _p(b, _u8p), _p(sfb, _u8p), M, N, K,
+                               _p(hi, _i64p), _p(lo, _u64p))
+    if nan:
+        raise ValueError("NaN scale code in exact GEMM input")
+    return [[(int(hi[i, j]) << 64) + int(lo[i, j]) for j in range(N)] for i in range(M)]
+
+
+def grouped_gemm(a, sfa, ga, b, sfb, gb, offsets, E, M_total, N, K, rows=None, cols=None):
+    a, sfa, b, sfb = (np.ascontiguousarray(t, dtype=np.uint8) for t in (a, sfa, b, sfb))
+    gb = np.ascontiguousarray(gb, dtype=np.float32)
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    r_arr, nr, r_ptr = _opt_idx(rows)
+    c_arr, nc, c_ptr = _opt_idx(cols)
+    nr = M_total if rows is None else nr
+    nc = N if cols is None else nc
+    y = np.zeros((nr, nc), dtype=np.float64)
+    ad = np.zeros((nr, nc), dtype=np.float64)
+    bad = lib().nvo_grouped_gemm_f64(_p(a, _u8p), _p(sfa, _u8p), float(ga), _p(b, _u8p),
+                                     _p(sfb, _u8p), _p(gb, _f32p), _p(off, _i32p), E, M_total,
+                                     N, K, r_ptr, nr, c_ptr, nc, _p(y, _f64p), _p(ad, _f64p))
+    if bad:
+        raise ValueError("malformed expert offsets")
+    return y, ad
+
+
+def within_tolerance(y_gpu: np.ndarray, y_ref: np.ndarray, absdot: np.ndarray,
+                     rel: float = 4e-3, absk: float = 1e-5):
+    """Per-element |y_gpu - y_ref| <= rel*|y_ref| + absk*sum_k|x^ w^|; returns (ok, worst ratio)."""
+    err = np.abs(np.asarray(y_gpu, dtype=np.float64) - y_ref)
+    bound = rel * np.abs(y_ref) + absk * absdot
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(bound > 0, err / bound, np.where(err > 0, np.inf, 0.0))
+    worst = float(np.max(ratio)) if ratio.size else 0.0
+    return bool(np.all(err <= bound)), worst
+
+
+def num_threads() -> int:
+    return int(lib().nvo_num_threads())
