@@ -1,0 +1,174 @@
+/*
+ * nvfp4.h - C ABI of the GB300 (sm_103a) NVFP4 block-scaled GEMM library.
+ *
+ * What is computed (the pages are cited by title and section):
+ *   "NVFP4 linear layer" (kernelindex, operation header): y = x @ W^T, where x
+ *   and W are FP4 (E2M1) values with FP8 E4M3FN scale factors, one scale per 16
+ *   consecutive K elements (sf_vec_size = 16, sf_k = K/16, in_features_half = K/2).
+ *   "The 3.7 PFLOPS Revelation" (magik.net, Input Knowledge item 2): two FP4
+ *   values per byte, so data tensors are [rows, K/2] and scale tensors [rows, K/16].
+ *   "The Moment of Recalibration" (magik.net, Input Knowledge) and "The Moment of
+ *   Synthesis" (magik.net, Reasoning): MoE layers of 256 experts with top-8
+ *   routing, each expert a small GEMM; grouped GEMM is the remedy.
+ *
+ * Conventions taken by this library where the pages are silent:
+ *   - Packed FP4: byte j of a row holds element 2j in bits 0-3 and 2j+1 in bits 4-7.
+ *   - Scale tensors are tiled: scale (r, c), c = k/16, lives at byte
+ *       ((r/128) * ceil(Kc/4) + c/4) * 512 + (r%32) * 16 + ((r%128)/32) * 4 + c%4,
+ *     Kc = K/16; the tensor has nvfp4_scale_bytes(rows, K) bytes, padding 0.
+ *   - Each tensor carries one FP32 global scale g in the decode direction:
+ *     value = E2M1(code) * E4M3(scale) * g. Quantisation uses g = amax/(6*448).
+ *   - y = bf16_rn((sum_k x^ w^) * g_a * g_b), accumulated in fp32 on the GPU.
+ *
+ * General rules for every entry point:
+ *   - Tensor arguments are DEVICE pointers owned by the caller; bf16 tensors are
+ *     passed as uint16_t bit patterns; scalars such as g are device fp32.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls only
+ *     enqueue work: they never synchronise and never allocate.
+ *   - The return value is NVFP4_OK or a negative nvfp4_status for arguments
+ *     rejected on the host (nothing is enqueued then) or a failed launch
+ *     (NVFP4_ERR_CUDA). Errors found on the device (malformed expert offsets, a
+ *     wait that timed out) are written to *dev_status when dev_status is not
+ *     NULL; the caller zeroes it beforehand and reads it after synchronising.
+ *   - Shapes: K % 64 == 0, N % 8 == 0, M >= 0, all sizes < 2^31. Data, scale and
+ *     output base pointers are 16-byte aligned (TMA). M == 0 is a no-op.
+ *   - The device must be compute capability 10.3 (GB300, sm_103a).
+ */
+#ifndef NVFP4_H_
+#define NVFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = -1,     /* null pointer, negative size */
+  NVFP4_ERR_UNSUPPORTED_SHAPE = -2, /* K % 64, N % 8, size limits */
+  NVFP4_ERR_ALIGNMENT = -3,       /* a base pointer is not 16-byte aligned */
+  NVFP4_ERR_ARCH = -4,            /* current device is not sm_103 */
+  NVFP4_ERR_CUDA = -5,            /* a CUDA call or launch failed */
+  NVFP4_ERR_WORKSPACE = -6,       /* workspace missing or too small */
+  NVFP4_ERR_TIMEOUT = -7,         /* device: a pipeline wait gave up (watchdog) */
+  NVFP4_ERR_BAD_OFFSETS = -8      /* device: expert_offsets not 0..M_total, non-decreasing */
+} nvfp4_status;
+
+/* Human-readable name of a status code. Never NULL. */
+const char* nvfp4_status_string(int status);
+
+/* Bytes of a tiled scale tensor for `rows` rows and K elements per row:
+ * ceil(rows/128)*128 * ceil(K/64)*4. Returns 0 for invalid sizes. */
+int64_t nvfp4_scale_bytes(int64_t rows, int64_t K);
+
+/*
+ * Tensor-wide amax of a bf16 tensor and its global scale. Not on the pages
+ * (they quantise "ahead of execution": "Blackwell NVFP4 GEMM" case page, What is
+ * this?); the recipe is the library's reading: g = amax / 2688 (6 * 448), and
+ * g = 1 when amax == 0.
+ *   x          device bf16 [n], 16-byte aligned
+ *   amax_out   device fp32 scalar, written (may be NULL)
+ *   g_out      device fp32 scalar, written (may be NULL)
+ *   workspace  device scratch of nvfp4_amax_workspace_bytes(n) bytes, 16-byte aligned
+ */
+size_t nvfp4_amax_workspace_bytes(int64_t n);
+int nvfp4_amax(const uint16_t* x, int64_t n, float* amax_out, float* g_out, void* workspace,
+               size_t workspace_bytes, void* stream);
+
+/*
+ * bf16 -> NVFP4 block quantisation (the secondary path; the pages exclude
+ * quantisation from their timings: "Blackwell NVFP4 GEMM" case page, What is this?).
+ * Per row r and 16-element block b, with g = *global_scale (device fp32, > 0):
+ *   s = E4M3_rn_satfinite((amax_b / 6) / g), q = E2M1_rn_satfinite(x / (E4M3(s) * g)),
+ *   all codes 0 when s == 0; every step one IEEE fp32 round-to-nearest-even op.
+ *   x        device bf16 [M, K] row-major, 16-byte aligned
+ *   q_out    device u8 [M, K/2]
+ *   sf_out   device u8, nvfp4_scale_bytes(M, K) bytes, tiled layout (padding written 0)
+ * Bit-exact with the library's CPU oracle.
+ */
+int nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, const float* global_scale, uint8_t* q_out,
+                   uint8_t* sf_out, void* stream);
+
+/*
+ * Dense NVFP4 GEMM, y = x @ W^T ("NVFP4 linear layer", kernelindex, operation header).
+ *   a, sfa, ga   x: packed [M, K/2], tiled scales nvfp4_scale_bytes(M, K), fp32 global scale
+ *   b, sfb, gb   W: packed [N, K/2], tiled scales nvfp4_scale_bytes(N, K), fp32 global scale
+ *   y            bf16 [M, N] row-major, written
+ *   workspace    may be NULL when nvfp4_gemm_workspace_bytes() returns 0 (it does today)
+ * Small M (decode) runs a weight-streaming split-K kernel, large M a persistent
+ * tcgen05 tile kernel; the result agrees with the oracle within
+ * |y - y_ref| <= 4e-3 |y_ref| + 1e-5 sum_k |x^_k w^_k|.
+ */
+size_t nvfp4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b, const uint8_t* sfb,
+               const float* gb, uint16_t* y, int64_t M, int64_t N, int64_t K, void* workspace,
+               size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * Grouped (MoE) NVFP4 GEMM: for each expert e and each row m with
+ * expert_offsets[e] <= m < expert_offsets[e+1], y[m, :] = x[m, :] @ W_e^T
+ * ("The Moment of Synthesis", magik.net, Reasoning: grouped GEMM over the
+ * per-expert GEMMs of ~16-32 tokens each).
+ *   a, sfa, ga       routed tokens, rows sorted by expert: packed [M_total, K/2],
+ *                    one tiled scale tensor over M_total rows, one global scale
+ *   b, sfb, gb       expert weights: packed [E, N, K/2]; scales [E] x nvfp4_scale_bytes(N, K)
+ *                    bytes back to back; gb device fp32 [E]
+ *   expert_offsets   device int32 [E+1], 0 = offsets[0] <= ... <= offsets[E] = M_total;
+ *                    checked on the device (NVFP4_ERR_BAD_OFFSETS in *dev_status, y untouched)
+ *   y                bf16 [M_total, N], written
+ *   workspace        device scratch of nvfp4_grouped_gemm_workspace_bytes(E, M_total, N, K)
+ *                    bytes, 256-byte aligned, contents need no initialisation
+ * Experts with no rows read none of their weights. Routing, the token gather
+ * and the weighted combine are the caller's.
+ */
+size_t nvfp4_grouped_gemm_workspace_bytes(int32_t E, int64_t M_total, int64_t N, int64_t K);
+int nvfp4_grouped_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b,
+                       const uint8_t* sfb, const float* gb, const int32_t* expert_offsets, int32_t E,
+                       int64_t M_total, int64_t N, int64_t K, uint16_t* y, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * Elementwise device encoders used by the quantiser, for exhaustive checks:
+ * fp32 -> E2M1 code (round to nearest even, saturating, sign kept) and
+ * fp32 -> E4M3FN code (round to nearest even, saturating to +-448).
+ *   v device fp32 [n]; out device u8 [n].
+ */
+int nvfp4_encode_e2m1(const float* v, int64_t n, uint8_t* out, void* stream);
+int nvfp4_encode_e4m3(const float* v, int64_t n, uint8_t* out, void* stream);
+
+/*
+ * Process-wide tuning overrides (0 restores the automatic choice). Used by the
+ * tests to force each kernel path and by benchmark sweeps. Not thread-safe with
+ * concurrent GEMM calls.
+ *   NVFP4_TUNE_DENSE_BN        dense tile width: 128 or 256
+ *   NVFP4_TUNE_DENSE_GRID      persistent CTAs of the dense kernel
+ *   NVFP4_TUNE_STREAM_MAX_M    largest M sent to the weight-streaming kernel (<= 128;
+ *                              -1 sends every M to the tile kernel)
+ *   NVFP4_TUNE_STREAM_SPLIT    split-K cluster size of the streaming kernel (1..8)
+ *   NVFP4_TUNE_STREAM_STAGES   pipeline depth of the streaming kernel (2..16)
+ *   NVFP4_TUNE_GROUPED_GRID    persistent CTAs of the grouped kernel
+ *   NVFP4_TUNE_GROUPED_STAGES  pipeline depth of the grouped kernel (2..16)
+ * Returns NVFP4_OK or NVFP4_ERR_INVALID_ARG.
+ */
+enum {
+  NVFP4_TUNE_DENSE_BN = 1,
+  NVFP4_TUNE_DENSE_GRID = 2,
+  NVFP4_TUNE_STREAM_MAX_M = 3,
+  NVFP4_TUNE_STREAM_SPLIT = 4,
+  NVFP4_TUNE_STREAM_STAGES = 5,
+  NVFP4_TUNE_GROUPED_GRID = 6,
+  NVFP4_TUNE_GROUPED_STAGES = 7
+};
+int nvfp4_tune(int key, int value);
+
+/* Number of kernel launches the last GEMM / grouped GEMM / quantize / amax call
+ * on this host thread enqueued (for launch accounting in benchmarks). */
+int nvfp4_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H_ */

@@ -1,0 +1,386 @@
+// C ABI: argument validation, TMA descriptor encoding, plan selection and
+// launches. Declarations and the contract of every entry point: include/nvfp4.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "nvfp4.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+
+using namespace nvfp4;
+
+namespace {
+
+constexpr int kAmaxPartials = 1024;
+constexpr int kGroupTileRows = kGroupTile;
+constexpr int kSmemLimit = 232448;
+
+thread_local int g_last_launches = 0;
+
+struct Tune {
+  int dense_bn = 0, dense_grid = 0, stream_max_m = 0, stream_split = 0, stream_stages = 0, grouped_grid = 0,
+      grouped_stages = 0;
+} g_tune;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct DevInfo {
+  int sms = 0;
+  bool ok = false;
+};
+
+int device_info(DevInfo& d) {
+  static DevInfo cache[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NVFP4_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev].sms == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    cache[dev].sms = sms;
+    cache[dev].ok = (major == 10 && minor == 3);
+  }
+  d = cache[dev];
+  return d.ok ? NVFP4_OK : NVFP4_ERR_ARCH;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D uint8 view [rows, cols] (cols bytes contiguous), 128-byte-swizzled boxes of
+// 128 bytes x box_rows; out-of-range elements read as zero.
+int encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return NVFP4_ERR_CUDA;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+
+int64_t pad16(int64_t v) { return (v + 15) / 16 * 16; }
+
+int pow2_at_least(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+}  // namespace
+
+extern "C" {
+
+const char* nvfp4_status_string(int s) {
+  switch (s) {
+    case NVFP4_OK: return "NVFP4_OK";
+    case NVFP4_ERR_INVALID_ARG: return "NVFP4_ERR_INVALID_ARG";
+    case NVFP4_ERR_UNSUPPORTED_SHAPE: return "NVFP4_ERR_UNSUPPORTED_SHAPE";
+    case NVFP4_ERR_ALIGNMENT: return "NVFP4_ERR_ALIGNMENT";
+    case NVFP4_ERR_ARCH: return "NVFP4_ERR_ARCH";
+    case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA";
+    case NVFP4_ERR_WORKSPACE: return "NVFP4_ERR_WORKSPACE";
+    case NVFP4_ERR_TIMEOUT: return "NVFP4_ERR_TIMEOUT";
+    case NVFP4_ERR_BAD_OFFSETS: return "NVFP4_ERR_BAD_OFFSETS";
+    default: return "NVFP4_UNKNOWN_STATUS";
+  }
+}
+
+int64_t nvfp4_scale_bytes(int64_t rows, int64_t K) {
+  if (rows < 0 || K < 0) return 0;
+  return (rows + 127) / 128 * 128 * ((K / 16 + 3) / 4 * 4);
+}
+
+int nvfp4_last_launch_count(void) { return g_last_launches; }
+
+int nvfp4_tune(int key, int value) {
+  switch (key) {
+    case NVFP4_TUNE_DENSE_BN:
+      if (value != 0 && value != 128 && value != 256) return NVFP4_ERR_INVALID_ARG;
+      g_tune.dense_bn = value;
+      return NVFP4_OK;
+    case NVFP4_TUNE_DENSE_GRID:
+      if (value < 0) return NVFP4_ERR_INVALID_ARG;
+      g_tune.dense_grid = value;
+      return NVFP4_OK;
+    case NVFP4_TUNE_STREAM_MAX_M:
+      if (value < -1 || value > 128) return NVFP4_ERR_INVALID_ARG;
+      g_tune.stream_max_m = value;
+      return NVFP4_OK;
+    case NVFP4_TUNE_STREAM_SPLIT:
+      if (value < 0 || value > 8) return NVFP4_ERR_INVALID_ARG;
+      g_tune.stream_split = value;
+      return NVFP4_OK;
+    case NVFP4_TUNE_STREAM_STAGES:
+      if (value != 0 && (value < 2 || value > 16)) return NVFP4_ERR_INVALID_ARG;
+      g_tune.stream_stages = value;
+      return NVFP4_OK;
+    case NVFP4_TUNE_GROUPED_GRID:
+      if (value < 0) return NVFP4_ERR_INVALID_ARG;
+      g_tune.grouped_grid = value;
+      return NVFP4_OK;
+    case NVFP4_TUNE_GROUPED_STAGES:
+      if (value != 0 && (value < 2 || value > 16)) return NVFP4_ERR_INVALID_ARG;
+      g_tune.grouped_stages = value;
+      return NVFP4_OK;
+    default:
+      return NVFP4_ERR_INVALID_ARG;
+  }
+}
+
+size_t nvfp4_amax_workspace_bytes(int64_t n) {
+  (void)n;
+  return kAmaxPartials * sizeof(float);
+}
+
+int nvfp4_amax(const uint16_t* x, int64_t n, float* amax_out, float* g_out, void* workspace, size_t workspace_bytes,
+               void* stream) {
+  g_last_launches = 0;
+  if (n < 0 || (n > 0 && !x)) return NVFP4_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < nvfp4_amax_workspace_bytes(n)) return NVFP4_ERR_WORKSPACE;
+  if (!aligned16(x) || !aligned16(workspace)) return NVFP4_ERR_ALIGNMENT;
+  DevInfo d;
+  int rc = device_info(d);
+  if (rc) return rc;
+  rc = from_cuda(launch_amax(x, n, amax_out, g_out, static_cast<float*>(workspace), kAmaxPartials,
+                             static_cast<cudaStream_t>(stream)));
+  g_last_launches = 2;
+  return rc;
+}
+
+int nvfp4_quantize(const uint16_t* x, int64_t M, int64_t K, const float* g, uint8_t* q, uint8_t* sf, void* stream) {
+  g_last_launches = 0;
+  if (M < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
+  if (K % 64 != 0 || M > kMaxDim || K > kMaxDim || (M + 127) / 128 > 65535 || K / 64 > kMaxDim)
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0 || K == 0) return NVFP4_OK;
+  if (!x || !g || !q || !sf) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return NVFP4_ERR_ALIGNMENT;
+  DevInfo d;
+  int rc = device_info(d);
+  if (rc) return rc;
+  rc = from_cuda(launch_quantize(x, M, K, g, q, sf, static_cast<cudaStream_t>(stream)));
+  g_last_launches = 1;
+  return rc;
+}
+
+int nvfp4_encode_e2m1(const float* v, int64_t n, uint8_t* out, void* stream) {
+  if (n < 0 || (n > 0 && (!v || !out))) return NVFP4_ERR_INVALID_ARG;
+  if (n == 0) return NVFP4_OK;
+  DevInfo d;
+  int rc = device_info(d);
+  if (rc) return rc;
+  return from_cuda(launch_encode(0, v, n, out, static_cast<cudaStream_t>(stream)));
+}
+
+int nvfp4_encode_e4m3(const float* v, int64_t n, uint8_t* out, void* stream) {
+  if (n < 0 || (n > 0 && (!v || !out))) return NVFP4_ERR_INVALID_ARG;
+  if (n == 0) return NVFP4_OK;
+  DevInfo d;
+  int rc = device_info(d);
+  if (rc) return rc;
+  return from_cuda(launch_encode(1, v, n, out, static_cast<cudaStream_t>(stream)));
+}
+
+size_t nvfp4_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  (void)M;
+  (void)N;
+  (void)K;
+  return 0;
+}
+
+static int check_gemm_shape(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N <= 0 || K <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (K % 64 != 0 || N % 8 != 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return NVFP4_OK;
+}
+
+int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b, const uint8_t* sfb,
+               const float* gb, uint16_t* y, int64_t M, int64_t N, int64_t K, void* workspace,
+               size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  g_last_launches = 0;
+  int rc = check_gemm_shape(M, N, K);
+  if (rc) return rc;
+  if (M == 0) return NVFP4_OK;
+  if (!a || !sfa || !ga || !b || !sfb || !gb || !y) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(y))
+    return NVFP4_ERR_ALIGNMENT;
+  DevInfo d;
+  rc = device_info(d);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  const int max_m = g_tune.stream_max_m == 0 ? 128 : g_tune.stream_max_m;
+  if (M <= max_m) {
+    // weight streaming: W on the MMA's 128-lane side, the M tokens on its N side
+    CUtensorMap tmW, tmX;
+    if ((rc = encode_2d(&tmW, b, N, K / 2, 128))) return rc;
+    if ((rc = encode_2d(&tmX, a, M, K / 2, 16))) return rc;
+    const int NT = static_cast<int>((N + 127) / 128);
+    const int KB = static_cast<int>((K + 255) / 256);
+    StreamArgs s = {};
+    s.sfw = sfb;
+    s.sfw_stride = 0;
+    s.sfx = sfa;
+    s.ga = ga;
+    s.gb = gb;
+    s.y = y;
+    s.status = dev_status;
+    s.M = static_cast<int>(M);
+    s.N = static_cast<int>(N);
+    s.K = static_cast<int>(K);
+    s.x_rows = static_cast<int>(pad16(M));
+    s.acc_cols = s.x_rows < 32 ? 32 : s.x_rows;
+    s.acc_bufs = 1;
+    int split = g_tune.stream_split;
+    if (split == 0) {
+      split = (2 * d.sms) / NT;
+      split = split < 1 ? 1 : (split > 8 ? 8 : split);
+    }
+    if (split > KB) split = KB;
+    s.split = split;
+    const int stage_bytes = stream_smem_bytes(1, s.x_rows) - 1536;
+    int stages = g_tune.stream_stages;
+    if (stages == 0) {
+      stages = (110 * 1024 - 1536) / stage_bytes;  // two CTAs per SM
+      const int tmem_room = (256 - s.acc_cols) / 32;
+      if (stages > tmem_room) stages = tmem_room;
+      if (stages < 2) stages = 2;
+    }
+    // split-K partials reuse the stage ring: it must hold x_rows x 128 fp32
+    while (split > 1 && stages * stage_bytes < s.x_rows * 512) ++stages;
+    if (stream_smem_bytes(stages, s.x_rows) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    s.stages = stages;
+    s.tmem_cols = pow2_at_least(s.acc_cols + 32 * stages);
+    if (s.tmem_cols > 512) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    rc = from_cuda(launch_stream(tmW, tmX, s, false, NT * split, st));
+    g_last_launches = 1;
+    return rc;
+  }
+
+  int bn = g_tune.dense_bn ? g_tune.dense_bn : (N <= 128 ? 128 : 256);
+  CUtensorMap tmA, tmB;
+  if ((rc = encode_2d(&tmA, a, M, K / 2, 128))) return rc;
+  if ((rc = encode_2d(&tmB, b, N, K / 2, bn))) return rc;
+  DenseArgs da = {sfa, sfb, ga, gb, y, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), dev_status};
+  const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
+  int grid = g_tune.dense_grid ? g_tune.dense_grid : d.sms;
+  if (grid > tiles) grid = static_cast<int>(tiles);
+  rc = from_cuda(launch_dense(tmA, tmB, da, bn, grid, st));
+  g_last_launches = 1;
+  return rc;
+}
+
+static int64_t grouped_max_tiles(int32_t E, int64_t M_total) { return (M_total + kGroupTileRows - 1) / kGroupTileRows + E; }
+
+static int64_t grouped_slab_offset(int32_t E, int64_t M_total) {
+  return (16 + grouped_max_tiles(E, M_total) * 16 + 255) / 256 * 256;
+}
+
+size_t nvfp4_grouped_gemm_workspace_bytes(int32_t E, int64_t M_total, int64_t N, int64_t K) {
+  (void)N;
+  if (E <= 0 || M_total < 0 || K <= 0) return 0;
+  return static_cast<size_t>(grouped_slab_offset(E, M_total) + grouped_max_tiles(E, M_total) * (K / 64) * 512);
+}
+
+int nvfp4_grouped_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b, const uint8_t* sfb,
+                       const float* gb, const int32_t* expert_offsets, int32_t E, int64_t M_total, int64_t N,
+                       int64_t K, uint16_t* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                       void* stream) {
+  g_last_launches = 0;
+  if (E <= 0) return NVFP4_ERR_INVALID_ARG;
+  int rc = check_gemm_shape(M_total, N, K);
+  if (rc) return rc;
+  if (static_cast<int64_t>(E) * N > kMaxDim || E > 16384) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (M_total == 0) return NVFP4_OK;
+  if (!a || !sfa || !ga || !b || !sfb || !gb || !expert_offsets || !y) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(y))
+    return NVFP4_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < nvfp4_grouped_gemm_workspace_bytes(E, M_total, N, K))
+    return NVFP4_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return NVFP4_ERR_ALIGNMENT;
+  DevInfo d;
+  rc = device_info(d);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* n_tiles = reinterpret_cast<int32_t*>(ws);
+  int4* tiles = reinterpret_cast<int4*>(ws + 16);
+  uint8_t* slabs = ws + grouped_slab_offset(E, M_total);
+  const int64_t words = M_total * (K / 64);
+  int prep_grid = static_cast<int>((words + 255) / 256);
+  if (prep_grid > 4 * d.sms) prep_grid = 4 * d.sms;
+  if (prep_grid < 1) prep_grid = 1;
+  rc = from_cuda(launch_grouped_prep(expert_offsets, E, static_cast<int>(M_total), static_cast<int>(K), sfa, n_tiles,
+                                     tiles, slabs, dev_status, prep_grid, st));
+  g_last_launches = 1;
+  if (rc) return rc;
+
+  CUtensorMap tmW, tmX;
+  if ((rc = encode_2d(&tmW, b, static_cast<uint64_t>(E) * N, K / 2, 128))) return rc;
+  if ((rc = encode_2d(&tmX, a, M_total, K / 2, 16))) return rc;
+  StreamArgs s = {};
+  s.sfw = sfb;
+  s.sfw_stride = nvfp4_scale_bytes(N, K);
+  s.sfx = slabs;
+  s.ga = ga;
+  s.gb = gb;
+  s.y = y;
+  s.tiles = tiles;
+  s.n_tiles = n_tiles;
+  s.status = dev_status;
+  s.M = static_cast<int>(M_total);
+  s.N = static_cast<int>(N);
+  s.K = static_cast<int>(K);
+  s.split = 1;
+  s.x_rows = kGroupTileRows;
+  s.acc_cols = kGroupTileRows;
+  s.acc_bufs = 2;
+  const int stage_bytes = stream_smem_bytes(1, s.x_rows) - 1536;
+  int stages = g_tune.grouped_stages;
+  if (stages == 0) stages = (kSmemLimit - 1536) / stage_bytes;
+  const int tmem_room = (512 - 2 * s.acc_cols) / 32;
+  if (stages > tmem_room) stages = tmem_room;
+  if (stages > 16) stages = 16;
+  if (stream_smem_bytes(stages, s.x_rows) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  s.stages = stages;
+  s.tmem_cols = pow2_at_least(2 * s.acc_cols + 32 * stages);
+  const int grid = g_tune.grouped_grid ? g_tune.grouped_grid : d.sms;
+  rc = from_cuda(launch_stream(tmW, tmX, s, true, grid, st));
+  g_last_launches = 2;
+  return rc;
+}
+
+}  // extern "C"

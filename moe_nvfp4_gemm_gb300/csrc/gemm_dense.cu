@@ -1,0 +1,237 @@
+// Dense NVFP4 GEMM for large M: y[M,N] = bf16((x^ . W^T^) * g_a * g_b).
+//
+// Operation: "NVFP4 linear layer" (kernelindex, operation header): y = x @ W^T,
+// both operands FP4 with FP8 E4M3FN scales per 16 elements.
+//
+// Persistent warp-specialised tcgen05 kernel, one CTA per SM, tile 128 x BN:
+//   warp 0      TMA producer: K-major 128-byte-swizzled data tiles (256 K per
+//               stage) and the matching 512-byte scale tiles (plain bulk copies)
+//               into a STAGES-deep shared-memory ring;
+//   warp 1      allocates TMEM; one lane copies the stage's scales into TMEM
+//               (tcgen05.cp) and issues 4 block-scaled MMAs (K = 64 each),
+//               accumulating in TMEM;
+//   warps 2-5   epilogue: TMEM -> registers, scale by g_a * g_b, bf16, store.
+// Every wait is bounded (globaltimer watchdog) and reports a timeout status.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+
+template <int BN, int STAGES>
+struct DenseCfg {
+  static constexpr int A_BYTES = 128 * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int GROUPS = BN / 128;  // 128-row scale tiles of B per stage
+  static constexpr int SFA_BYTES = 4 * 512;
+  static constexpr int SFB_BYTES = GROUPS * 4 * 512;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int SF_COLS = 16 + 16 * GROUPS;  // TMEM scale columns per stage
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static_assert(BN + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_dense(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const DenseArgs p) {
+  using C = DenseCfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 128);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int M = p.M, N = p.N, K = p.K;
+  const int mt = (M + 127) / 128, nt = (N + BN - 1) / BN, tiles = mt * nt;
+  const int KB = (K + 255) / 256;
+  const int64_t KC4 = K / 64;  // 512-byte scale tiles per 128 rows
+  const int n_rowblk = (N + 127) / 128;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();
+      int s = 0;
+      uint32_t ph = 0;
+      int issued_phase[STAGES];
+      for (int i = 0; i < STAGES; ++i) issued_phase[i] = -1;
+      for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+        const int m_blk = t % mt, n_blk = t / mt;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) break;
+          const int nsub = min(4, (K - kb * 256) / 64);
+          uint8_t* st = smem + s * C::STAGE_BYTES;
+          int ngroups = 0;
+#pragma unroll
+          for (int g = 0; g < C::GROUPS; ++g) ngroups += (n_blk * C::GROUPS + g < n_rowblk) ? 1 : 0;
+          mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES + nsub * 512 * (1 + ngroups));
+          tma_load_2d(st, &tmA, &full[s], kb * 128, m_blk * 128, pol);
+          tma_load_2d(st + C::A_BYTES, &tmB, &full[s], kb * 128, n_blk * BN, pol);
+          bulk_load(st + C::A_BYTES + C::B_BYTES, p.sfa + (m_blk * KC4 + kb * 4) * 512, nsub * 512, &full[s], pol);
+#pragma unroll
+          for (int g = 0; g < C::GROUPS; ++g) {
+            const int rb = n_blk * C::GROUPS + g;
+            if (rb < n_rowblk)
+              bulk_load(st + C::A_BYTES + C::B_BYTES + C::SFA_BYTES + g * 2048, p.sfb + (rb * KC4 + kb * 4) * 512,
+                        nsub * 512, &full[s], pol);
+          }
+          issued_phase[s] = ph;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      // Let every copy this CTA started land before shared memory is released.
+      for (int i = 0; i < STAGES; ++i)
+        if (issued_phase[i] >= 0) {
+          volatile int32_t dummy = 0;
+          mbar_wait(&full[i], issued_phase[i], &dummy);
+        }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_nvf4(128, BN);
+      int s = 0;
+      uint32_t ph = 0, acc_ph = 0;
+      for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+        if (!mbar_wait(tempty, acc_ph ^ 1, abort_flag)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&full[s], ph, abort_flag)) break;
+          tc_fence_after();
+          const int nsub = min(4, (K - kb * 256) / 64);
+          const uint32_t a_addr = smem_u32(smem + s * C::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + C::A_BYTES;
+          const uint32_t sfa_addr = b_addr + C::B_BYTES;
+          const uint32_t sfb_addr = sfa_addr + C::SFA_BYTES;
+          const uint32_t sf_col = tmem + BN + s * C::SF_COLS;
+          for (int kk = 0; kk < nsub; ++kk) {
+            tc_cp_32x128b_x4(sf_col + kk * 4, desc_sf(sfa_addr + kk * 512));
+#pragma unroll
+            for (int g = 0; g < C::GROUPS; ++g)
+              tc_cp_32x128b_x4(sf_col + 16 + kk * 4 * C::GROUPS + g * 4, desc_sf(sfb_addr + g * 2048 + kk * 512));
+          }
+          const uint64_t adesc = desc_sw128(a_addr), bdesc = desc_sw128(b_addr);
+          for (int kk = 0; kk < nsub; ++kk)
+            tc_mma_nvf4(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, sf_col + kk * 4,
+                        sf_col + 16 + kk * 4 * C::GROUPS, (kb | kk) != 0);
+          tc_commit(&empty[s]);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        tc_commit(tfull);
+        acc_ph ^= 1;
+      }
+      // All MMAs issued by this thread complete before TMEM is released.
+      tc_commit(drain);
+      volatile int32_t dummy = 0;
+      mbar_wait(drain, 0, &dummy);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    const float alpha = __ldg(p.ga) * __ldg(p.gb);
+    uint32_t acc_ph = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+      const int m_blk = t % mt, n_blk = t / mt;
+      if (!mbar_wait(tfull, acc_ph, abort_flag)) break;
+      tc_fence_after();
+      const int row = m_blk * 128 + q * 32 + lane;
+      uint16_t* yrow = p.y + static_cast<int64_t>(row) * N;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r0[16], r1[16];
+        const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + c;
+        tmem_ld16(ta, r0);
+        tmem_ld16(ta + 16, r1);
+        tmem_ld_wait();
+        const int col = n_blk * BN + c;
+        if (row < M) {
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int cc = col + h * 8;
+            if (cc < N) {
+              const uint32_t* r = (h < 2) ? r0 : r1;
+              const int o = (h & 1) * 8;
+              st_global_v4(yrow + cc, pack_bf16x2(__uint_as_float(r[o + 0]) * alpha, __uint_as_float(r[o + 1]) * alpha),
+                           pack_bf16x2(__uint_as_float(r[o + 2]) * alpha, __uint_as_float(r[o + 3]) * alpha),
+                           pack_bf16x2(__uint_as_float(r[o + 4]) * alpha, __uint_as_float(r[o + 5]) * alpha),
+                           pack_bf16x2(__uint_as_float(r[o + 6]) * alpha, __uint_as_float(r[o + 7]) * alpha));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty);
+      acc_ph ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && *abort_flag) report_status(p.status, kStatusTimeout);
+}
+
+template <int BN, int STAGES>
+static cudaError_t launch_dense_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const DenseArgs& a, int grid,
+                                  cudaStream_t st) {
+  using C = DenseCfg<BN, STAGES>;
+  static bool configured = false;  // attribute is per function; set before the first launch
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_dense<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  k_gemm_dense<BN, STAGES><<<grid, 192, C::SMEM_BYTES, st>>>(tmA, tmB, a);
+  return cudaGetLastError();
+}
+
+// bn selects the tile width (128 or 256); grid is the persistent CTA count.
+cudaError_t launch_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const DenseArgs& a, int bn, int grid,
+                         cudaStream_t st) {
+  if (bn == 256) return launch_dense_t<256, 4>(tmA, tmB, a, grid, st);
+  return launch_dense_t<128, 6>(tmA, tmB, a, grid, st);
+}
+
+}  // namespace nvfp4

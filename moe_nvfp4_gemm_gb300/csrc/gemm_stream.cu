@@ -1,0 +1,413 @@
+// Weight-streaming NVFP4 GEMM for small token counts: decode-M dense layers and
+// the grouped MoE path (per-expert GEMMs over routed tokens).
+//
+// Operations: "NVFP4 linear layer" (kernelindex, operation header), y = x @ W^T;
+// MoE decode shape from "The Moment of Recalibration" (magik.net, Input
+// Knowledge: 256 experts, top-8) and "The Moment of Synthesis" (magik.net,
+// Reasoning: ~32 x 2048 x 6144 per expert, grouped GEMM as the lever for small
+// per-expert M; persistent grouped GEMM in the Broader Narrative Arc of "The
+// Moment of Recalibration").
+//
+// Swap-AB: the MMA's M side (128 TMEM lanes) holds 128 weight rows, its N side
+// holds the tokens (padded to 16), so no token is padded to 128 rows. One TMA
+// stream reads each weight tile once; the tokens come from L2.
+//   dense decode: grid = (N/128) x S CTAs in clusters of S along K; each CTA
+//     reduces its K slice in TMEM, the S partials are summed through DSMEM.
+//   grouped: a persistent grid walks (token tile, weight tile) items built by
+//     k_grouped_prep (ragged per-expert counts, empty experts skipped); each
+//     item streams one expert's 128-row weight tile over all of K.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+
+struct StreamLayout {
+  int stage_bytes, x_off, sfw_off, sfx_off;
+  __host__ __device__ StreamLayout(int x_rows) {
+    x_off = 16384;
+    sfw_off = x_off + x_rows * 128;
+    sfx_off = sfw_off + 2048;
+    stage_bytes = sfx_off + 2048;
+  }
+};
+
+DEVI void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+DEVI uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+DEVI float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+struct Item {
+  int wt;      // 128-row weight tile
+  int e;       // expert (0 for dense)
+  int row0;    // first token row
+  int rows;    // token rows (<= x_rows)
+  int slab;    // grouped scale slab
+  int kb0, kb1;
+};
+
+template <bool GROUPED>
+DEVI bool get_item(const StreamArgs& p, int i, int n_items, int NT, int KB, Item& it) {
+  if (i >= n_items) return false;
+  if (GROUPED) {
+    const int tile = i / NT;
+    const int4 t = __ldg(p.tiles + tile);
+    it.wt = i % NT;
+    it.e = t.x;
+    it.row0 = t.y;
+    it.rows = t.z;
+    it.slab = t.w;
+    it.kb0 = 0;
+    it.kb1 = KB;
+  } else {
+    it.wt = i / p.split;
+    const int sp = i % p.split;
+    it.e = 0;
+    it.row0 = 0;
+    it.rows = p.M;
+    it.slab = 0;
+    it.kb0 = static_cast<int>((static_cast<int64_t>(KB) * sp) / p.split);
+    it.kb1 = static_cast<int>((static_cast<int64_t>(KB) * (sp + 1)) / p.split);
+  }
+  return true;
+}
+
+template <bool GROUPED>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                  const StreamArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const StreamLayout L(p.x_rows);
+  const int STAGES = p.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * L.stage_bytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;  // [2]
+  uint64_t* tempty = tfull + 2;      // [2]
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmX);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int N = p.N, K = p.K;
+  const int NT = (N + 127) / 128;
+  const int KB = (K + 255) / 256;
+  const int64_t KC4 = K / 64;
+  int n_items, first, stride;
+  if (GROUPED) {
+    n_items = __ldg(p.n_tiles) * NT;
+    first = blockIdx.x;
+    stride = gridDim.x;
+  } else {
+    n_items = NT * p.split;
+    first = blockIdx.x;
+    stride = n_items;  // one item per CTA
+  }
+  const uint32_t sf_base = tmem + p.acc_bufs * p.acc_cols;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+      int s = 0;
+      uint32_t ph = 0;
+      int issued_phase[16];
+      for (int i = 0; i < 16; ++i) issued_phase[i] = -1;
+      Item it;
+      for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it) && !*abort_flag; i += stride) {
+        const int n16 = (it.rows + 15) >> 4;
+        const int64_t wrow0 = static_cast<int64_t>(it.e) * N + it.wt * 128;
+        const uint8_t* sfw = p.sfw + it.e * p.sfw_stride + static_cast<int64_t>(it.wt) * KC4 * 512;
+        const uint8_t* sfx = p.sfx + static_cast<int64_t>(it.slab) * KC4 * 512;
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) break;
+          const int nsub = min(4, (K - kb * 256) / 64);
+          uint8_t* st = smem + s * L.stage_bytes;
+          mbar_arrive_expect_tx(&full[s], 16384 + n16 * 2048 + nsub * 1024);
+          tma_load_2d(st, &tmW, &full[s], kb * 128, static_cast<int32_t>(wrow0), pol_w);
+          for (int j = 0; j < n16; ++j)
+            tma_load_2d(st + L.x_off + j * 2048, &tmX, &full[s], kb * 128, it.row0 + j * 16, pol_x);
+          bulk_load(st + L.sfw_off, sfw + kb * 2048, nsub * 512, &full[s], pol_w);
+          bulk_load(st + L.sfx_off, sfx + kb * 2048, nsub * 512, &full[s], pol_x);
+          issued_phase[s] = ph;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      for (int i = 0; i < STAGES; ++i)
+        if (issued_phase[i] >= 0) {
+          volatile int32_t dummy = 0;
+          mbar_wait(&full[i], issued_phase[i], &dummy);
+        }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int s = 0, buf = 0;
+      uint32_t ph = 0, acc_ph[2] = {0, 0};
+      Item it;
+      for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it) && !*abort_flag; i += stride) {
+        const int n_mma = ((it.rows + 15) >> 4) * 16;
+        const uint32_t idesc = idesc_nvf4(128, n_mma);
+        const uint32_t acc = tmem + buf * p.acc_cols;
+        if (!mbar_wait(&tempty[buf], acc_ph[buf] ^ 1, abort_flag)) break;
+        tc_fence_after();
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
+          if (!mbar_wait(&full[s], ph, abort_flag)) break;
+          tc_fence_after();
+          const int nsub = min(4, (K - kb * 256) / 64);
+          const uint32_t w_addr = smem_u32(smem + s * L.stage_bytes);
+          const uint32_t x_addr = w_addr + L.x_off;
+          const uint32_t sf_col = sf_base + s * 32;
+          for (int kk = 0; kk < nsub; ++kk) {
+            tc_cp_32x128b_x4(sf_col + kk * 4, desc_sf(w_addr + L.sfw_off + kk * 512));
+            tc_cp_32x128b_x4(sf_col + 16 + kk * 4, desc_sf(w_addr + L.sfx_off + kk * 512));
+          }
+          const uint64_t wdesc = desc_sw128(w_addr), xdesc = desc_sw128(x_addr);
+          for (int kk = 0; kk < nsub; ++kk)
+            tc_mma_nvf4(acc, wdesc + 2 * kk, xdesc + 2 * kk, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4,
+                        (kb != it.kb0) || (kk != 0));
+          tc_commit(&empty[s]);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        tc_commit(&tfull[buf]);
+        acc_ph[buf] ^= 1;
+        buf = (buf + 1 == p.acc_bufs) ? 0 : buf + 1;
+      }
+      tc_commit(drain);
+      volatile int32_t dummy = 0;
+      mbar_wait(drain, 0, &dummy);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3;
+    const float ga = __ldg(p.ga);
+    int buf = 0;
+    uint32_t acc_ph[2] = {0, 0};
+    float* red = reinterpret_cast<float*>(smem);  // split-K partials (stage memory, reused)
+    Item it;
+    for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it); i += stride) {
+      if (!mbar_wait(&tfull[buf], acc_ph[buf], abort_flag)) break;
+      tc_fence_after();
+      const float alpha = ga * __ldg(p.gb + it.e);
+      const int wrow = it.wt * 128 + q * 32 + lane;  // output column
+      const int n_mma = ((it.rows + 15) >> 4) * 16;
+      const bool has_k = it.kb1 > it.kb0;
+      for (int c = 0; c < n_mma; c += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem + buf * p.acc_cols + (static_cast<uint32_t>(q * 32) << 16) + c, r);
+        tmem_ld_wait();
+        if (!GROUPED && p.split > 1) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) red[(c + j) * 128 + q * 32 + lane] = has_k ? __uint_as_float(r[j]) : 0.0f;
+        } else if (wrow < N) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = c + j;
+            if (tok < it.rows) {
+              const float v = __uint_as_float(r[j]) * alpha;
+              p.y[static_cast<int64_t>(it.row0 + tok) * N + wrow] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(v));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[buf]);
+      acc_ph[buf] ^= 1;
+      buf = (buf + 1 == p.acc_bufs) ? 0 : buf + 1;
+    }
+  }
+
+  if (!GROUPED && p.split > 1) {
+    // Sum the S partial tiles of this cluster through distributed shared memory;
+    // CTA rank r finishes tokens r, r + S, ...
+    cluster_sync_all();
+    if (warp >= 2) {
+      const int q = warp & 3;
+      const uint32_t rank = cluster_rank();
+      const int wt = blockIdx.x / p.split;
+      const int wrow = wt * 128 + q * 32 + lane;
+      const float alpha = __ldg(p.ga) * __ldg(p.gb);
+      const uint32_t red_addr = smem_u32(smem);
+      for (int tok = rank; tok < p.M; tok += p.split) {
+        float v = 0.0f;
+        for (int c = 0; c < p.split; ++c) v += ld_dsmem_f32(red_addr + (tok * 128 + q * 32 + lane) * 4, c);
+        if (wrow < N) p.y[static_cast<int64_t>(tok) * N + wrow] = __bfloat16_as_ushort(__float2bfloat16_rn(v * alpha));
+      }
+    }
+    cluster_sync_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) report_status(p.status, kStatusTimeout);
+}
+
+// ---- grouped preparation ------------------------------------------------------------
+
+// Validates expert_offsets, lists the token tiles (<= kGroupTile rows of one
+// expert each; experts without rows get none) and gathers each tile's token
+// scales into its own slab in the 128-row tiled layout, rows starting at 0.
+// Workspace: [0] n_tiles, [16..) int4 tiles[max_tiles], then the slabs.
+__global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict__ offsets, int E, int M_total, int K,
+                                                      const uint8_t* __restrict__ sfx, int32_t* n_tiles_out,
+                                                      int4* __restrict__ tiles, uint8_t* __restrict__ slabs,
+                                                      int32_t* status) {
+  extern __shared__ int32_t sh[];  // offsets[E+1], tile_base[E+1]
+  int32_t* off = sh;
+  int32_t* tbase = sh + (E + 1);
+  __shared__ int bad;
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    off[e] = offsets[e];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (off[e + 1] < off[e]) bad = 1;
+  if (threadIdx.x == 0 && (off[0] != 0 || off[E] != M_total)) bad = 1;
+  __syncthreads();
+  if (bad) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      *n_tiles_out = 0;
+      report_status(status, kStatusBadOffsets);
+    }
+    return;
+  }
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      tbase[e] = acc;
+      acc += (off[e + 1] - off[e] + kGroupTile - 1) / kGroupTile;
+    }
+    tbase[E] = acc;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      const int cnt = off[e + 1] - off[e];
+      for (int t = 0; t * kGroupTile < cnt; ++t)
+        tiles[tbase[e] + t] = make_int4(e, off[e] + t * kGroupTile, min(kGroupTile, cnt - t * kGroupTile), tbase[e] + t);
+    }
+    if (threadIdx.x == 0) *n_tiles_out = tbase[E];
+  }
+  // scale gather: one 4-byte word = (row m, four consecutive 16-element blocks)
+  const int64_t KC4 = K / 64;
+  const int64_t words = static_cast<int64_t>(M_total) * KC4;
+  for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < words; w += (int64_t)gridDim.x * blockDim.x) {
+    const int m = static_cast<int>(w / KC4);
+    const int c4 = static_cast<int>(w % KC4);
+    int lo = 0, hi = E;  // expert e with off[e] <= m < off[e+1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (off[mid] <= m) lo = mid; else hi = mid;
+    }
+    while (off[lo + 1] <= m) ++lo;  // skip empty experts sharing the same offset
+    const int j = m - off[lo];
+    const int tile = tbase[lo] + j / kGroupTile;
+    const int r = j % kGroupTile;
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(sfx + ((m / 128) * KC4 + c4) * 512 + (m % 32) * 16 +
+                                                          ((m % 128) / 32) * 4);
+    *reinterpret_cast<uint32_t*>(slabs + (tile * KC4 + c4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4) = v;
+  }
+}
+
+// ---- host launchers -------------------------------------------------------------------
+
+template <bool GROUPED>
+static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, int grid,
+                                   cudaStream_t st) {
+  const StreamLayout L(a.x_rows);
+  const int smem = a.stages * L.stage_bytes + 1024 + 512;
+  cudaError_t e = cudaFuncSetAttribute(k_gemm_stream<GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  int nattr = 0;
+  if (!GROUPED && a.split > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = a.split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    nattr = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = nattr;
+  e = cudaLaunchKernelEx(&cfg, k_gemm_stream<GROUPED>, tmW, tmX, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+int stream_smem_bytes(int stages, int x_rows) { return stages * StreamLayout(x_rows).stage_bytes + 1024 + 512; }
+
+cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, bool grouped, int grid,
+                          cudaStream_t st) {
+  return grouped ? launch_stream_t<true>(tmW, tmX, a, grid, st) : launch_stream_t<false>(tmW, tmX, a, grid, st);
+}
+
+cudaError_t launch_grouped_prep(const int32_t* offsets, int E, int M_total, int K, const uint8_t* sfx,
+                                int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
+                                cudaStream_t st) {
+  const int smem = 2 * (E + 1) * 4;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_grouped_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  k_grouped_prep<<<grid, 256, smem, st>>>(offsets, E, M_total, K, sfx, n_tiles, tiles, slabs, status);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,56 @@
+// Launch interfaces shared by the C ABI (capi.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+struct DenseArgs {
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  const float* ga;
+  const float* gb;
+  uint16_t* y;
+  int M, N, K;
+  int32_t* status;
+};
+
+struct StreamArgs {
+  const uint8_t* sfw;      // weight scales (grouped: expert e at sfw + e * sfw_stride)
+  int64_t sfw_stride;
+  const uint8_t* sfx;      // dense: token scales; grouped: scale slabs per token tile
+  const float* ga;
+  const float* gb;         // grouped: gb[e]
+  uint16_t* y;
+  const int4* tiles;       // grouped: (expert, first row, rows, slab)
+  const int32_t* n_tiles;  // grouped: device count of tiles
+  int32_t* status;
+  int M;                   // dense: tokens; grouped: M_total
+  int N, K;
+  int split;               // dense: cluster size along K
+  int stages;
+  int x_rows;              // token rows reserved per stage (multiple of 16)
+  int acc_cols;            // TMEM columns per accumulator buffer
+  int acc_bufs;
+  int tmem_cols;
+};
+
+constexpr int kGroupTile = 64;  // tokens of one expert per grouped work item (MMA N <= 64)
+
+cudaError_t launch_amax(const uint16_t* x, int64_t n, float* amax_out, float* g_out, float* partial,
+                        int max_partials, cudaStream_t st);
+cudaError_t launch_quantize(const uint16_t* x, int64_t M, int64_t K, const float* g, uint8_t* q, uint8_t* sf,
+                            cudaStream_t st);
+cudaError_t launch_encode(int which, const float* v, int64_t n, uint8_t* out, cudaStream_t st);
+cudaError_t launch_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const DenseArgs& a, int bn, int grid,
+                         cudaStream_t st);
+cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, bool grouped,
+                          int grid, cudaStream_t st);
+cudaError_t launch_grouped_prep(const int32_t* offsets, int E, int M_total, int K, const uint8_t* sfx,
+                                int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
+                                cudaStream_t st);
+int stream_smem_bytes(int stages, int x_rows);
+
+}  // namespace nvfp4

@@ -1,0 +1,189 @@
+// bf16 -> NVFP4 quantisation: the tensor-wide amax / global scale and the
+// per-16-element block quantiser (E4M3 block scale + packed E2M1 codes, scales
+// written in the 128-row x 4-column tiled layout).
+//
+// Formats: "NVFP4 linear layer" (kernelindex, operation header) - FP4 values
+// with FP8 E4M3FN scales, one per 16 elements; "The 3.7 PFLOPS Revelation"
+// (magik.net, Input Knowledge item 2) - two FP4 values per byte, [rows, K/2].
+// Recipe (the pages fix none; this is the library's stated reading):
+//   g = amax / 2688 (1 if amax == 0); s = E4M3_rn_sat((amax_blk / 6) / g);
+//   q = E2M1_rn_sat(x / (E4M3(s) * g)), sign kept; q = 0 when s == 0.
+// Every float step is one IEEE round-to-nearest operation (true division).
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+DEVI uint32_t e4m3_encode(float t) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(t));
+  return r & 0xFFu;
+}
+
+DEVI float e4m3_decode(uint32_t code) {
+  uint32_t h2;
+  uint16_t in = static_cast<uint16_t>(code & 0xFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+// Two E2M1 codes in one byte: `lo` in bits 0-3, `hi` in bits 4-7.
+DEVI uint32_t e2m1x2_encode(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+DEVI float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+DEVI float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ---- amax ------------------------------------------------------------------------
+
+// Per-CTA partial maxima of |x| over a grid-stride sweep (16-byte loads).
+__global__ void __launch_bounds__(256) k_amax_partial(const uint16_t* __restrict__ x, int64_t n,
+                                                      float* __restrict__ partial) {
+  float m = 0.0f;
+  const int64_t nvec = n / 8;
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nvec;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    uint4 v = __ldg(xv + i);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16lo(w[j])), fabsf(bf16hi(w[j]))));
+  }
+  for (int64_t i = nvec * 8 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    m = fmaxf(m, fabsf(__uint_as_float(static_cast<uint32_t>(x[i]) << 16)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (threadIdx.x == 0) partial[blockIdx.x] = m;
+  }
+}
+
+// Reduces the partial maxima; writes amax and the decode-direction global scale.
+__global__ void __launch_bounds__(256) k_amax_final(const float* __restrict__ partial, int np,
+                                                    float* amax_out, float* g_out) {
+  float m = 0.0f;
+  for (int i = threadIdx.x; i < np; i += blockDim.x) m = fmaxf(m, partial[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+    m = fmaxf(m, red[0]);
+    if (amax_out) *amax_out = m;
+    if (g_out) *g_out = (m == 0.0f) ? 1.0f : __fdiv_rn(m, 2688.0f);
+  }
+}
+
+// ---- block quantiser -----------------------------------------------------------
+
+// One CTA = 128 rows x 64 columns (one 512-byte scale tile); one thread = one
+// 16-element block. Thread i: row i/4 of the tile, block i%4. A warp reads 8
+// rows x 128 contiguous bytes; the 512 scale bytes leave as one coalesced tile.
+__global__ void __launch_bounds__(512) k_quantize(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                  const float* __restrict__ gptr,
+                                                  uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  __shared__ uint32_t tile[128];
+  const int r_local = threadIdx.x >> 2;
+  const int c_local = threadIdx.x & 3;
+  const int64_t row = static_cast<int64_t>(blockIdx.y) * 128 + r_local;
+  const int64_t col4 = blockIdx.x;  // which group of four 16-element blocks
+  const int64_t blk = col4 * 4 + c_local;
+  const float g = __ldg(gptr);
+  uint32_t s = 0;
+  if (row < M) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + row * K + blk * 16);
+    uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+    uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float f[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      f[2 * j] = bf16lo(w[j]);
+      f[2 * j + 1] = bf16hi(w[j]);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    const float t = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
+    s = e4m3_encode(t);
+    uint32_t packed[2] = {0u, 0u};
+    if (s != 0) {
+      const float d = __fmul_rn(e4m3_decode(s), g);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t b = e2m1x2_encode(__fdiv_rn(f[2 * j], d), __fdiv_rn(f[2 * j + 1], d));
+        packed[j >> 2] |= b << ((j & 3) * 8);
+      }
+    }
+    uint2* dst = reinterpret_cast<uint2*>(q + row * (K / 2) + blk * 8);
+    *dst = make_uint2(packed[0], packed[1]);
+  }
+  // scale byte (r, c) of the tile sits at (r % 32) * 16 + (r / 32) * 4 + c
+  reinterpret_cast<uint8_t*>(tile)[(r_local & 31) * 16 + (r_local >> 5) * 4 + c_local] =
+      static_cast<uint8_t>(s);
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    const int64_t kc4 = K / 64;
+    uint32_t* out = reinterpret_cast<uint32_t*>(sf + (static_cast<int64_t>(blockIdx.y) * kc4 + col4) * 512);
+    out[threadIdx.x] = tile[threadIdx.x];
+  }
+}
+
+// Elementwise encoders, exposed for exhaustive checks of the device conversions.
+__global__ void k_encode_e2m1(const float* __restrict__ v, int64_t n, uint8_t* __restrict__ out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = static_cast<uint8_t>(e2m1x2_encode(v[i], 0.0f) & 0xF);
+}
+
+__global__ void k_encode_e4m3(const float* __restrict__ v, int64_t n, uint8_t* __restrict__ out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = static_cast<uint8_t>(e4m3_encode(v[i]));
+}
+
+// ---- host launchers ----------------------------------------------------------------
+
+cudaError_t launch_amax(const uint16_t* x, int64_t n, float* amax_out, float* g_out, float* partial,
+                        int max_partials, cudaStream_t st) {
+  int64_t want = (n / 8 + 255) / 256;
+  int grid = static_cast<int>(want < 1 ? 1 : (want > max_partials ? max_partials : want));
+  k_amax_partial<<<grid, 256, 0, st>>>(x, n, partial);
+  k_amax_final<<<1, 256, 0, st>>>(partial, grid, amax_out, g_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const uint16_t* x, int64_t M, int64_t K, const float* g, uint8_t* q,
+                            uint8_t* sf, cudaStream_t st) {
+  dim3 grid(static_cast<unsigned>(K / 64), static_cast<unsigned>((M + 127) / 128));
+  k_quantize<<<grid, 512, 0, st>>>(x, M, K, g, q, sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode(int which, const float* v, int64_t n, uint8_t* out, cudaStream_t st) {
+  int64_t want = (n + 255) / 256;
+  int grid = static_cast<int>(want < 1 ? 1 : (want > 65535 ? 65535 : want));
+  if (which == 0)
+    k_encode_e2m1<<<grid, 256, 0, st>>>(v, n, out);
+  else
+    k_encode_e4m3<<<grid, 256, 0, st>>>(v, n, out);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

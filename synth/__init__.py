@@ -21,12 +21,52 @@ Fisher-Yates), rows sorted by expert.
 """
 from __future__ import annotations
 
+import ctypes
+import os
+import subprocess
+import threading
+
 import numpy as np
 
 _GOLDEN = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
-_CHUNK = 1 << 22
+
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "synth_gen.c")
+_LIB = os.path.join(_HERE, "_build", "libsynth.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compiles the C form of the generator (same definition, OpenMP for speed)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    base = ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-shared", "-fPIC", "-o",
+            _LIB + ".tmp", _SRC, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+def _c():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            L.syn_normal_bf16.argtypes = [ctypes.c_uint64, ctypes.c_int64, ctypes.c_int64,
+                                          ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                          ctypes.c_void_p]
+            L.syn_uniform.argtypes = [ctypes.c_uint64, ctypes.c_int64, ctypes.c_int64,
+                                      ctypes.c_void_p]
+            _lib = L
+    return _lib
 
 
 def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
@@ -41,9 +81,10 @@ def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
 
 
 def uniform01(seed: int, start: int, count: int) -> np.ndarray:
-    """Uniforms in (0, 1] as float64."""
-    z = splitmix64(seed, start, count)
-    return ((z >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+    """Uniforms in (0, 1] as float64 (draws start .. start+count-1 of stream `seed`)."""
+    out = np.empty(count, dtype=np.float64)
+    _c().syn_uniform(seed, start, count, out.ctypes.data)
+    return out
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -62,13 +103,7 @@ def normal_bf16(shape, seed: int, std: float = 1.0, outlier_p: float = 0.0,
     """Seeded N(0, std^2) tensor with optional outliers, as bf16 bit patterns (uint16)."""
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16)
-    for s in range(0, n, _CHUNK):
-        c = min(_CHUNK, n - s)
-        u = uniform01(seed, 3 * s, 3 * c).reshape(c, 3)
-        v = np.sqrt(-2.0 * np.log(u[:, 0])) * np.cos(2.0 * np.pi * u[:, 1]) * std
-        if outlier_p > 0.0:
-            v = np.where(u[:, 2] <= outlier_p, v * outlier_mult, v)
-        out[s:s + c] = f32_to_bf16_bits(v.astype(np.float32))
+    _c().syn_normal_bf16(seed, 0, n, std, outlier_p, outlier_mult, out.ctypes.data)
     return out.reshape(shape)
 
 
@@ -114,17 +149,16 @@ def dense_inputs(M: int, N: int, K: int, seed: int, x_std=1.0, x_outlier=0.0, w_
     return x, w
 
 
-def moe_inputs(tokens: int, experts: int, topk: int, N: int, K: int, seed: int,
-               x_std=1.0, w_std=0.02, n_experts_materialised=None):
-    """Token activations gathered into expert-sorted rows, plus per-expert weights.
+def moe_tokens(tokens: int, experts: int, topk: int, K: int, seed: int, x_std=1.0):
+    """Routed token activations, gathered into expert-sorted rows.
 
-    Returns (a_rows [M_total,K] bf16 bits, w [E_m,N,K] bf16 bits, offsets[E+1],
-    token_of_row). `n_experts_materialised` limits how many expert weight tensors
-    are drawn (tests at reduced size); routing always spans `experts`.
+    Returns (a_rows [tokens*topk, K] bf16 bits, offsets[E+1], token_of_row).
     """
     tok, _, offsets = route_topk(tokens, experts, topk, 1000 + seed)
     x = normal_bf16((tokens, K), 2 * seed, x_std)
-    a_rows = x[tok]
-    e_m = experts if n_experts_materialised is None else n_experts_materialised
-    w = normal_bf16((e_m, N, K), 2 * seed + 1, w_std)
-    return a_rows, w, offsets, tok
+    return x[tok], offsets, tok
+
+
+def moe_expert_weight(e: int, N: int, K: int, seed: int, w_std=0.02) -> np.ndarray:
+    """Expert e's weight [N, K] as bf16 bits (its own stream, so experts can be drawn one by one)."""
+    return normal_bf16((N, K), 100000 + 1000 * seed + e, w_std)

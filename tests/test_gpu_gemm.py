@@ -1,0 +1,115 @@
+"""GPU parity of the dense NVFP4 GEMM (tile kernel and weight-streaming kernel)
+against the oracle, element by element, through the C ABI.
+
+Tolerance (per element): |y - y_ref| <= 4e-3 |y_ref| + 1e-5 sum_k |x^_k w^_k|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_nvfp4_gemm_gb300 as m
+import oracle
+import synth
+from tests.helpers import Operand, check_gemm, dense_case, dev, scalar, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _reset_tuning():
+    yield
+    for key in range(1, 8):
+        m.nvfp4_tune(key, 0)
+
+
+def _run(A, B, status=None):
+    y = m.nvfp4_gemm(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, A.rows, B.rows, A.K, dev_status=status)
+    torch.cuda.synchronize()
+    return y
+
+
+def test_tiny_workload_both_kernels():
+    # 128 x 128 x 256, x and W ~ N(0, 1), seed 0
+    A, B = dense_case(128, 128, 256, 0)
+    m.nvfp4_tune(m.NVFP4_TUNE_STREAM_MAX_M, -1)
+    check_gemm(_run(A, B), A, B)
+    m.nvfp4_tune(m.NVFP4_TUNE_STREAM_MAX_M, 128)
+    check_gemm(_run(A, B), A, B)
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("M,N,K", [
+    (256, 256, 256), (300, 264, 320), (129, 512, 1024), (1000, 136, 576), (384, 768, 2048)])
+def test_tile_kernel_shapes(bn, M, N, K):
+    A, B = dense_case(M, N, K, 11, 1.0, 1e-3, 0.02)
+    m.nvfp4_tune(m.NVFP4_TUNE_STREAM_MAX_M, -1)
+    m.nvfp4_tune(m.NVFP4_TUNE_DENSE_BN, bn)
+    check_gemm(_run(A, B), A, B)
+
+
+def test_tile_kernel_persistent_loop_small_grid():
+    # fewer CTAs than tiles: every CTA walks several tiles through the TMEM handoff
+    A, B = dense_case(640, 1024, 512, 12, 1.0, 1e-3, 0.02)
+    m.nvfp4_tune(m.NVFP4_TUNE_STREAM_MAX_M, -1)
+    m.nvfp4_tune(m.NVFP4_TUNE_DENSE_GRID, 3)
+    check_gemm(_run(A, B), A, B)
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("M,N,K", [(1, 256, 2048), (16, 384, 2048), (32, 128, 4096), (77, 264, 1088),
+                                   (128, 512, 512)])
+def test_stream_kernel_shapes(split, M, N, K):
+    A, B = dense_case(M, N, K, 13, 1.0, 1e-3, 0.02)
+    m.nvfp4_tune(m.NVFP4_TUNE_STREAM_SPLIT, split)
+    check_gemm(_run(A, B), A, B)
+
+
+def test_identity_gives_exact_weights():
+    K = 256
+    M, N = 128, 256
+    codes = np.zeros((M, K), dtype=np.uint8)
+    codes[np.arange(M), np.arange(M)] = 0x2
+    A = Operand(synth.f32_to_bf16_bits(np.eye(M, K, dtype=np.float32)))
+    B = Operand(synth.normal_bf16((N, K), 5, 0.02))
+    for max_m in (-1, 128):
+        m.nvfp4_tune(m.NVFP4_TUNE_STREAM_MAX_M, max_m)
+        y = _run(A, B)
+        ref, _ = oracle.gemm(A.q, A.sf, A.g, B.q, B.sf, B.g, M, N, K)
+        ref_bf16 = synth.f32_to_bf16_bits(ref.astype(np.float32))
+        got = y.view(torch.int16).cpu().numpy().view(np.uint16)
+        # ref values are short dyadics (exact in fp32), so bf16 rounding is unique
+        assert np.array_equal(got, ref_bf16)
+
+
+@pytest.mark.parametrize("M", [1, 16, 32])
+def test_decode_workload_full_size(M):
+    # N = K = 8192, x ~ N(0,1) + 0.1% x20, W ~ N(0, 0.02); all rows, sampled columns
+    A, B = dense_case(M, 8192, 8192, 2, 1.0, 1e-3, 0.02)
+    y = _run(A, B)
+    cols = np.random.default_rng(M).choice(8192, 512, replace=False)
+    check_gemm(y, A, B, cols=cols)
+
+
+def test_square_workload_sampled():
+    # M = N = K = 8192 in the benchmark's launch configuration; sampled rows x cols
+    A, B = dense_case(8192, 8192, 8192, 1, 1.0, 1e-3, 0.02)
+    y = _run(A, B)
+    rng = np.random.default_rng(0)
+    rows = np.concatenate([[0, 127, 128, 8191], rng.choice(8192, 60, replace=False)])
+    cols = np.concatenate([[0, 255, 256, 8191], rng.choice(8192, 124, replace=False)])
+    check_gemm(y, A, B, rows=rows, cols=cols)
+    # properties at full size: finite everywhere
+    assert torch.isfinite(y.float()).all()
+
+
+def test_status_untouched_on_success():
+    A, B = dense_case(64, 128, 256, 3)
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    _run(A, B, st)
+    assert st.item() == 0
+
+
+def test_empty_m_is_noop():
+    A, B = dense_case(1, 128, 256, 4)
+    y = torch.full((0, 128), 7.0, dtype=torch.bfloat16, device=dev())
+    m.nvfp4_gemm(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, 0, 128, 256, y=y)

@@ -1,0 +1,114 @@
+"""GPU parity of the grouped (MoE) NVFP4 GEMM against the oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import moe_nvfp4_gemm_gb300 as m
+import oracle
+import synth
+from tests.helpers import dev, scalar, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _reset_tuning():
+    yield
+    for key in range(1, 8):
+        m.nvfp4_tune(key, 0)
+
+
+class Grouped:
+    def __init__(self, counts, N, K, seed, a_rows=None, w=None):
+        E = len(counts)
+        self.E, self.N, self.K = E, N, K
+        self.off = np.zeros(E + 1, dtype=np.int32)
+        self.off[1:] = np.cumsum(counts)
+        self.Mt = int(self.off[-1])
+        if a_rows is None:
+            a_rows = synth.normal_bf16((max(self.Mt, 1), K), 2 * seed, 1.0)[: self.Mt]
+        if w is None:
+            w = lambda e: synth.moe_expert_weight(e, N, K, seed)
+        self.qa, self.sfa, self.ga = oracle.quantize(a_rows) if self.Mt else (None, None, 1.0)
+        sfb_bytes = oracle.scale_bytes(N, K)
+        self.qb = np.empty((E, N, K // 2), dtype=np.uint8)
+        self.sfb = np.empty((E, sfb_bytes), dtype=np.uint8)
+        self.gb = np.empty(E, dtype=np.float32)
+        for e in range(E):
+            self.qb[e], self.sfb[e], self.gb[e] = oracle.quantize(w(e))
+
+    def run(self, status=None, offsets=None):
+        off = self.off if offsets is None else offsets
+        y = m.nvfp4_grouped_gemm(to_dev(self.qa), to_dev(self.sfa), scalar(self.ga), to_dev(self.qb),
+                                 to_dev(self.sfb), to_dev(self.gb), to_dev(off), self.E, self.Mt,
+                                 self.N, self.K, dev_status=status)
+        torch.cuda.synchronize()
+        return y
+
+    def check(self, y, rows=None, cols=None):
+        yr, ad = oracle.grouped_gemm(self.qa, self.sfa, self.ga, self.qb, self.sfb, self.gb, self.off,
+                                     self.E, self.Mt, self.N, self.K, rows=rows, cols=cols)
+        yg = y.float().cpu().numpy()
+        if rows is not None:
+            yg = yg[np.asarray(rows)]
+        if cols is not None:
+            yg = yg[:, np.asarray(cols)]
+        ok, worst = oracle.within_tolerance(yg, yr, ad)
+        assert ok, f"grouped parity failed: worst ratio {worst}"
+
+
+@pytest.mark.parametrize("counts", [
+    (3, 0, 17, 1, 0, 9),                 # ragged, empty experts
+    (64, 65, 63, 1, 127, 128, 129, 0),   # tile-boundary counts
+    (0, 0, 300, 0),                      # one expert owns every row
+    (5,),                                # single expert
+])
+def test_grouped_ragged_counts(counts):
+    g = Grouped(counts, 256, 512, 21)
+    g.check(g.run())
+
+
+def test_grouped_ragged_n_and_k():
+    g = Grouped((10, 40, 0, 7), 136, 1088, 22)
+    g.check(g.run())
+
+
+def test_grouped_small_persistent_grid_and_stages():
+    g = Grouped((33, 2, 70, 16, 16), 384, 768, 23)
+    m.nvfp4_tune(m.NVFP4_TUNE_GROUPED_GRID, 5)
+    m.nvfp4_tune(m.NVFP4_TUNE_GROUPED_STAGES, 2)
+    g.check(g.run())
+
+
+def test_grouped_moe_workload_sampled():
+    # 256 experts, 512 tokens routed top-8 uniformly (~16 rows / expert), K = 6144, N = 4096
+    a_rows, off, tok = synth.moe_tokens(512, 256, 8, 6144, 3)
+    counts = np.diff(off)
+    g = Grouped(tuple(counts), 4096, 6144, 3, a_rows=a_rows,
+                w=lambda e: synth.moe_expert_weight(e, 4096, 6144, 3))
+    assert np.array_equal(g.off, off)
+    y = g.run()
+    rng = np.random.default_rng(1)
+    rows = np.concatenate([[0, g.Mt - 1], rng.choice(g.Mt, 30, replace=False)])
+    cols = np.concatenate([[0, 4095], rng.choice(4096, 62, replace=False)])
+    g.check(y, rows=rows, cols=cols)
+
+
+def test_grouped_bad_offsets_reported_and_output_untouched():
+    g = Grouped((4, 4, 4), 128, 256, 24)
+    bad = g.off.copy()
+    bad[1], bad[2] = bad[2], bad[1]
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    y = torch.full((g.Mt, g.N), 3.0, dtype=torch.bfloat16, device=dev())
+    m.nvfp4_grouped_gemm(to_dev(g.qa), to_dev(g.sfa), scalar(g.ga), to_dev(g.qb), to_dev(g.sfb),
+                         to_dev(g.gb), to_dev(bad), g.E, g.Mt, g.N, g.K, y=y, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == -8
+    assert (y.float() == 3.0).all()
+    bad = g.off.copy()
+    bad[-1] -= 1
+    st.zero_()
+    m.nvfp4_grouped_gemm(to_dev(g.qa), to_dev(g.sfa), scalar(g.ga), to_dev(g.qb), to_dev(g.sfb),
+                         to_dev(g.gb), to_dev(bad), g.E, g.Mt, g.N, g.K, y=y, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == -8

@@ -1,0 +1,105 @@
+"""GPU parity of the quantisation path (amax, global scale, block quantiser,
+device encoders) against the oracle: bit-exact, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.helpers import dev, to_dev
+
+pytestmark = pytest.mark.gpu
+m = pytest.importorskip("moe_nvfp4_gemm_gb300")
+
+
+def test_encode_e2m1_exhaustive_decision_range():
+    lo = int(np.float32(0.125).view(np.uint32))
+    hi = int(np.float32(16.0).view(np.uint32))
+    bits = np.arange(lo, hi, dtype=np.uint32)
+    v = bits.view(np.float32)
+    for sign in (1, -1):
+        vv = (v * sign).astype(np.float32)
+        got = m.nvfp4_encode_e2m1(to_dev(vv)).cpu().numpy()
+        assert np.array_equal(got, oracle.e2m1_encode_array(vv))
+
+
+def test_encode_e2m1_random_bit_patterns():
+    rng = np.random.default_rng(1)
+    v = rng.integers(0, 2**32, size=1 << 22, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    v = np.ascontiguousarray(v[np.isfinite(v)])
+    got = m.nvfp4_encode_e2m1(to_dev(v)).cpu().numpy()
+    assert np.array_equal(got, oracle.e2m1_encode_array(v))
+
+
+def test_encode_e4m3_matches_oracle():
+    # every float32 in [2^-12, 512) plus neighbourhoods of every rounding midpoint
+    lo = int(np.float32(2.0 ** -12).view(np.uint32))
+    hi = int(np.float32(512.0).view(np.uint32))
+    v = np.arange(lo, hi, 7, dtype=np.uint32).view(np.float32)
+    mids = []
+    for c in range(0, 0x7E):
+        mb = int(np.float32((oracle.e4m3_value(c) + oracle.e4m3_value(c + 1)) / 2).view(np.uint32))
+        mids.append(np.arange(mb - 64, mb + 65, dtype=np.uint32))
+    v = np.concatenate([v, np.concatenate(mids).view(np.float32), np.float32([0, 448, 464, 1e30])])
+    got = m.nvfp4_encode_e4m3(to_dev(v)).cpu().numpy()
+    assert np.array_equal(got, oracle.e4m3_encode_array(v))
+
+
+def _quantize_and_compare(xb, g_fixed=None):
+    x = to_dev(xb)
+    amax, g = m.nvfp4_amax(x)
+    if g_fixed is not None:
+        g = torch.tensor([g_fixed], dtype=torch.float32, device=dev())
+    q, sf = m.nvfp4_quantize(x, g)
+    qo, sfo, go = oracle.quantize(xb, g_fixed)
+    torch.cuda.synchronize()
+    assert np.float32(amax.item()) == np.float32(oracle.amax(xb))
+    assert np.float32(g.item()) == go
+    qg, sfg = q.cpu().numpy(), sf.cpu().numpy()
+    bad = np.argwhere(qg != qo)
+    assert bad.size == 0, f"{len(bad)} code bytes differ, first at {bad[:4].tolist()}"
+    assert np.array_equal(sfg, sfo)
+
+
+@pytest.mark.parametrize("M,K,seed,std,out", [
+    (128, 256, 0, 1.0, 0.0),       # the tiny workload's x
+    (1, 64, 1, 1.0, 0.0),          # single row, single scale tile column
+    (200, 512, 2, 0.02, 1e-3),     # ragged row tile
+    (333, 1088, 3, 3.0, 1e-2),     # ragged rows, K not a multiple of 256
+])
+def test_quantize_bit_exact(M, K, seed, std, out):
+    _quantize_and_compare(synth.normal_bf16((M, K), seed, std, out))
+
+
+def test_quantize_adversarial_blocks():
+    K = 256
+    rows = []
+    # ties of the E2M1 grid after division by a power-of-two block scale
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0] * 2, dtype=np.float32)
+    rows.append(np.concatenate([ties, -ties] * 8))
+    rows.append(np.zeros(K, dtype=np.float32))                       # all-zero blocks
+    one = np.zeros(K, dtype=np.float32)
+    one[::16] = np.float32(3.0)                                       # single nonzero per block
+    rows.append(one)
+    rows.append(np.full(K, 1e30, dtype=np.float32))                   # saturating blocks
+    tiny = np.zeros(K, dtype=np.float32)
+    tiny[::7] = np.float32(1e-30)                                     # scale underflows to 0
+    rows.append(tiny)
+    rows.append(np.where(np.arange(K) % 2 == 0, -1e-6, 2.0).astype(np.float32))  # -0 codes
+    x = np.stack(rows)
+    xb = synth.f32_to_bf16_bits(x)
+    # a power-of-two global scale keeps every block scale exact (ties stay ties)
+    _quantize_and_compare(xb, np.float32(2.0 ** -6))
+    _quantize_and_compare(xb)
+
+
+def test_quantize_prefill_size_bit_exact():
+    # the prefill workload's activations: 4096 x 8192 bf16, N(0,1) + 0.1% outliers x20
+    xb = synth.normal_bf16((4096, 8192), 8, 1.0, 1e-3)
+    _quantize_and_compare(xb)
+
+
+def test_amax_zero_tensor_gives_unit_scale():
+    x = torch.zeros(1000, dtype=torch.bfloat16, device=dev())
+    amax, g = m.nvfp4_amax(x)
+    assert amax.item() == 0.0 and g.item() == 1.0
