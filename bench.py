@@ -1,0 +1,460 @@
+"""NVFP4 GEMM benchmark on GB300.
+
+Headline workload: the square NVFP4 linear layer y = x . W^T, M = N = K = 8192
+(x ~ N(0,1) with 0.1% outliers x20, W ~ N(0, 0.02), both quantised per 16-K
+block to E2M1 + E4M3 scales + an FP32 global scale), bf16 output. One step is one
+nvfp4_gemm call on operands already resident in HBM; the timed loop rotates over
+4 distinct input/output sets (302 MB of operands > the 129 MB L2). The pages
+exclude quantisation from their GEMM timings ("Blackwell NVFP4 GEMM" case page,
+What is this?), so does the headline; the quantiser is timed on its own in the
+breakdown, next to the decode, MoE-grouped and prefill workloads.
+
+Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle instead
+(bounded row samples of the same workload on the host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 GEMM TFLOPS & % of GB300 dense FP4 peak; decode/grouped weight GB/s vs HBM"
+WORKLOAD = "square NVFP4 linear M=N=K=8192 (x N(0,1)+0.1% x20, W N(0,0.02)), bf16 out"
+SQ = 8192
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense ratio (fp4 13.5 PF vs bf16 2.25 PF)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-breakdown", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def reduce_max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over the process group (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            def pick(keys):
+                for k in keys:
+                    if k in d and isinstance(d[k], (int, float)):
+                        return float(d[k])
+                return None
+            hbm = pick(["hbm_gbs", "hbm_GBs"])
+            bf16 = pick(["bf16_tflops"])
+            bf16s = pick(["bf16_tflops_sustained"])
+            if hbm and bf16:
+                return {"hbm": hbm, "bf16": bf16, "bf16_sustained": bf16s or bf16, "source": "measured"}
+        except Exception:
+            pass
+    return {"hbm": FALLBACK_HBM_GBS, "bf16": FALLBACK_BF16_TFLOPS, "bf16_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"nvfp4_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        busy = [s for s in sm if s > 0]
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "moe_nvfp4_gemm_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    ent = d.get(kernel)
+    if not ent or ent.get("csrc_hash") != csrc_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle arm
+
+
+def cpu_oracle_gemm_rate(target_s: float):
+    """Times the float64 oracle on a bounded row sample of the square workload."""
+    import oracle
+    import synth
+    K = SQ
+    x = synth.normal_bf16((64, K), 2 * 1, 1.0, 1e-3)
+    w = synth.normal_bf16((SQ, K), 2 * 1 + 1, 0.02)
+    qa, sfa, ga = oracle.quantize(x)
+    qb, sfb, gb = oracle.quantize(w)
+    t0 = time.perf_counter()
+    oracle.gemm(qa, sfa, ga, qb, sfb, gb, 64, SQ, K, rows=[0])
+    t1 = time.perf_counter() - t0
+    rows = int(max(1, min(64, target_s / max(t1, 1e-3))))
+    t0 = time.perf_counter()
+    oracle.gemm(qa, sfa, ga, qb, sfb, gb, 64, SQ, K, rows=list(range(rows)))
+    dt = time.perf_counter() - t0
+    tflops = 2.0 * rows * SQ * K / dt / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{rows} full output rows of the 8192^3 GEMM ({rows}x8192 outputs, K=8192), "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args):
+    rank, local, world = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    K = SQ
+    x = synth.normal_bf16((16, K), 2, 1.0, 1e-3)
+    w = synth.normal_bf16((SQ, K), 3, 0.02)
+    qa, sfa, ga = oracle.quantize(x)
+    qb, sfb, gb = oracle.quantize(w)
+    rows_per_step = 1
+    for _ in range(args.warmup):
+        oracle.gemm(qa, sfa, ga, qb, sfb, gb, 16, SQ, K, rows=[0])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.gemm(qa, sfa, ga, qb, sfb, gb, 16, SQ, K, rows=[i % 16])
+    dt = time.perf_counter() - t0
+    tflops = 2.0 * rows_per_step * SQ * K * args.steps / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": "one output row (8192 outputs, K=8192) per step"},
+            "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": "one output row of the square GEMM per step"},
+            "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU arm
+
+
+def main():
+    args = parse()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import moe_nvfp4_gemm_gb300 as m
+    import synth
+
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+    fp4_peak = peaks["bf16"] * FP4_OVER_BF16  # TFLOP/s
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    def quantize_dev(bf16_dev):
+        amax, g = m.nvfp4_amax(bf16_dev)
+        q, sf = m.nvfp4_quantize(bf16_dev, g)
+        return q, sf, g
+
+    # ---- square workload: 4 rotating sets --------------------------------------------------
+    xb, wb = synth.dense_inputs(SQ, SQ, SQ, 1, 1.0, 1e-3, 0.02)
+    xa, sfa, ga = quantize_dev(to_dev(xb))
+    wq, sfb, gb = quantize_dev(to_dev(wb))
+    del xb, wb
+    R = 4
+    sets = [(xa.clone(), sfa.clone(), ga.clone(), wq.clone(), sfb.clone(), gb.clone(),
+             torch.empty((SQ, SQ), dtype=torch.bfloat16, device=dev)) for _ in range(R)]
+    op_bytes = sum(t.numel() * t.element_size() for t in sets[0][:6])
+    flops = 2.0 * SQ ** 3
+
+    def gemm(i):
+        a, sa, g1, b, sb, g2, y = sets[i % R]
+        m.nvfp4_gemm(a, sa, g1, b, sb, g2, SQ, SQ, SQ, y=y)
+        return m.nvfp4_last_launch_count()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for i in range(args.warmup):
+        gemm(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_all0, t_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    torch.cuda.synchronize()
+    t_all0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        launches += gemm(i)
+        ends[i].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t_all0.elapsed_time(t_all1)
+    total_ms = reduce_max_over_ranks(total_ms, world, dev)
+    per_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    ms_per_step = total_ms / args.steps
+    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers ------------------------------------
+    host_in = [t.cpu().pin_memory() for t in sets[0][:6]]
+    host_out = torch.empty((SQ, SQ), dtype=torch.bfloat16).pin_memory()
+    dev_in = [t.clone() for t in sets[0][:6]]
+    y_e2e = torch.empty((SQ, SQ), dtype=torch.bfloat16, device=dev)
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        m.nvfp4_gemm(dev_in[0], dev_in[1], dev_in[2], dev_in[3], dev_in[4], dev_in[5], SQ, SQ, SQ,
+                     y=y_e2e)
+        host_out.copy_(y_e2e, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    clocks = sampler.stop()
+
+    # ---- breakdown of the other workloads ---------------------------------------------------
+    breakdown = {}
+    if not args.no_breakdown and rank == 0:
+        del sets, dev_in, host_in, host_out, y_e2e
+        torch.cuda.empty_cache()
+        breakdown = run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak)
+
+    achieved = flops / (per_launch_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": SQ, "N": SQ, "K": SQ,
+                   "l2": f"rotating {R} input/output sets ({R * op_bytes / 1e6:.0f} MB of operands > 129 MB L2)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
+                     "frac": achieved / fp4_peak, "traffic": profiled_traffic("k_gemm_dense"),
+                     "kernel": "k_gemm_dense<256,4>",
+                     "peak_source": f"{peaks['source']} bf16 {peaks['bf16']:.0f} TFLOP/s x {FP4_OVER_BF16:g} (nominal fp4/bf16)"},
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "breakdown": breakdown,
+    }
+    if rank == 0 and world == 1 or rank == 0:
+        try:
+            line["cpu_baseline"] = cpu_oracle_gemm_rate(args.cpu_seconds) if world == 1 else None
+        except Exception as ex:  # the baseline is reported, never required
+            line["cpu_baseline"] = {"error": str(ex)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def time_launches(fn, n, stream, warm=3):
+    """Median device time (ms) of fn() over n launches, CUDA events on the launching stream."""
+    import torch
+    for i in range(warm):
+        fn(i)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(ev):
+        a.record(stream)
+        fn(i)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
+def run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak):
+    import torch
+    out = {}
+    hbm = peaks["hbm"]
+    # decode: M in {1, 16, 32}, N = K = 8192; 8 rotating weight copies (302 MB > L2)
+    w = synth.normal_bf16((SQ, SQ), 2 * 2 + 1, 0.02)
+    wq, sfw, gw = quantize_dev(to_dev(w))
+    del w
+    copies = [(wq.clone(), sfw.clone()) for _ in range(8)]
+    wbytes = wq.numel() + sfw.numel()
+    for M in (1, 16, 32):
+        x = synth.normal_bf16((M, SQ), 2 * 2, 1.0, 1e-3)
+        xa, sfa, ga = quantize_dev(to_dev(x))
+        y = torch.empty((M, SQ), dtype=torch.bfloat16, device=dev)
+        ms = time_launches(lambda i: m.nvfp4_gemm(xa, sfa, ga, copies[i % 8][0], copies[i % 8][1], gw,
+                                                  M, SQ, SQ, y=y), 200, stream)
+        gbs = wbytes / (ms * 1e-3) / 1e9
+        out[f"decode_M{M}"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm,
+                               "bytes": wbytes}
+    del copies, wq, sfw
+    # MoE grouped: 256 experts, 512 tokens top-8 (~16 rows/expert), K = 6144, N = 4096
+    E, N, K = 256, 4096, 6144
+    a_rows, off, tok = synth.moe_tokens(512, E, 8, K, 3)
+    Mt = int(off[-1])
+    qa, sfa, ga = quantize_dev(to_dev(a_rows))
+    qb = torch.empty((E, N, K // 2), dtype=torch.uint8, device=dev)
+    sfb_bytes = m.nvfp4_scale_bytes(N, K)
+    sfb = torch.empty((E, sfb_bytes), dtype=torch.uint8, device=dev)
+    gb = torch.empty(E, dtype=torch.float32, device=dev)
+    for e in range(E):
+        wq, ws, g = quantize_dev(to_dev(synth.moe_expert_weight(e, N, K, 3)))
+        qb[e].copy_(wq)
+        sfb[e].copy_(ws)
+        gb[e:e + 1].copy_(g)
+    off_d = to_dev(off)
+    y = torch.empty((Mt, N), dtype=torch.bfloat16, device=dev)
+    ws_bytes = m.nvfp4_grouped_gemm_workspace_bytes(E, Mt, N, K)
+    wsp = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ms = time_launches(lambda i: m.nvfp4_grouped_gemm(qa, sfa, ga, qb, sfb, gb, off_d, E, Mt, N, K,
+                                                      y=y, workspace=wsp), 30, stream)
+    hit = int((np.diff(off) > 0).sum())
+    mbytes = hit * (N * K // 2 + sfb_bytes)
+    gbs = mbytes / (ms * 1e-3) / 1e9
+    out["moe_grouped"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
+                          "bytes": mbytes, "tflops": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12}
+    del qb, sfb, wsp
+    torch.cuda.empty_cache()
+    # prefill: quantize x (4096 x 8192) on the GPU, GEMM against pre-quantised W (28672 x 8192)
+    Mp, Np, Kp = 4096, 28672, 8192
+    x = to_dev(synth.normal_bf16((Mp, Kp), 2 * 4, 1.0, 1e-3))
+    wq, sfw, gw = quantize_dev(to_dev(synth.normal_bf16((Np, Kp), 2 * 4 + 1, 0.02)))
+    wcopies = [(wq, sfw), (wq.clone(), sfw.clone())]
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    g = torch.empty(1, dtype=torch.float32, device=dev)
+    q = torch.empty((Mp, Kp // 2), dtype=torch.uint8, device=dev)
+    sf = torch.empty(m.nvfp4_scale_bytes(Mp, Kp), dtype=torch.uint8, device=dev)
+    aws = torch.empty(m.nvfp4_amax_workspace_bytes(Mp * Kp), dtype=torch.uint8, device=dev)
+    yp = torch.empty((Mp, Np), dtype=torch.bfloat16, device=dev)
+    m.nvfp4_amax(x, amax, g, aws)
+    ms_q = time_launches(lambda i: m.nvfp4_quantize(x, g, q, sf), 50, stream)
+    ms_amax = time_launches(lambda i: m.nvfp4_amax(x, amax, g, aws), 50, stream)
+    ms_g = time_launches(lambda i: m.nvfp4_gemm(q, sf, g, wcopies[i % 2][0], wcopies[i % 2][1], gw,
+                                                Mp, Np, Kp, y=yp), 20, stream)
+
+    def together(i):
+        m.nvfp4_amax(x, amax, g, aws)
+        m.nvfp4_quantize(x, g, q, sf)
+        m.nvfp4_gemm(q, sf, g, wcopies[i % 2][0], wcopies[i % 2][1], gw, Mp, Np, Kp, y=yp)
+
+    ms_t = time_launches(together, 20, stream)
+    qbytes = Mp * Kp * 2 + Mp * Kp // 2 + m.nvfp4_scale_bytes(Mp, Kp)
+    out["prefill"] = {
+        "quantize_us": ms_q * 1e3, "quantize_GBps": qbytes / (ms_q * 1e-3) / 1e9,
+        "quantize_hbm_frac": qbytes / (ms_q * 1e-3) / 1e9 / hbm, "quantize_bytes": qbytes,
+        "amax_us": ms_amax * 1e3, "amax_GBps": Mp * Kp * 2 / (ms_amax * 1e-3) / 1e9,
+        "gemm_us": ms_g * 1e3, "gemm_tflops": 2.0 * Mp * Np * Kp / (ms_g * 1e-3) / 1e12,
+        "gemm_frac": 2.0 * Mp * Np * Kp / (ms_g * 1e-3) / 1e12 / fp4_peak,
+        "together_us": ms_t * 1e3}
+    return out
+
+
+if __name__ == "__main__":
+    main()
