@@ -115,6 +115,18 @@ def nvfp4_last_launch_count() -> int:
     return int(lib().nvfp4_last_launch_count())
 
 
+def nvfp4_amax_workspace_bytes(n: int) -> int:
+    return int(lib().nvfp4_amax_workspace_bytes(n))
+
+
+def nvfp4_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().nvfp4_gemm_workspace_bytes(M, N, K))
+
+
+def nvfp4_status_string(status: int) -> str:
+    return lib().nvfp4_status_string(status).decode()
+
+
 def nvfp4_amax(x: torch.Tensor, amax_out=None, g_out=None, workspace=None, stream=None):
     """Returns (amax, g) as 1-element fp32 CUDA tensors; g = amax / 2688 (1 if amax == 0)."""
     _cuda(x, torch.bfloat16, "x")
