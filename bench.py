@@ -375,6 +375,28 @@ def time_launches(fn, n, stream, warm=3):
     return statistics.median(a.elapsed_time(b) for a, b in ev)
 
 
+def time_graph(fn, calls, reps, stream):
+    """Device time (ms) per fn() call: `calls` calls captured in one CUDA graph, replayed
+    `reps` times between two events (host launch overhead excluded)."""
+    import torch
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(calls):
+            fn(i)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (calls * reps)
+
+
 def run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak):
     import torch
     out = {}
@@ -389,11 +411,13 @@ def run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak):
         x = synth.normal_bf16((M, SQ), 2 * 2, 1.0, 1e-3)
         xa, sfa, ga = quantize_dev(to_dev(x))
         y = torch.empty((M, SQ), dtype=torch.bfloat16, device=dev)
-        ms = time_launches(lambda i: m.nvfp4_gemm(xa, sfa, ga, copies[i % 8][0], copies[i % 8][1], gw,
-                                                  M, SQ, SQ, y=y), 200, stream)
+        fn = lambda i: m.nvfp4_gemm(xa, sfa, ga, copies[i % 8][0], copies[i % 8][1], gw, M, SQ, SQ, y=y)
+        ms = time_graph(fn, 16, 20, stream)
+        ms_eager = time_launches(fn, 100, stream)
         gbs = wbytes / (ms * 1e-3) / 1e9
         out[f"decode_M{M}"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm,
-                               "bytes": wbytes}
+                               "bytes": wbytes, "timing": "CUDA graph of 16 calls over 8 weight copies",
+                               "us_eager_per_launch_events": ms_eager * 1e3}
     del copies, wq, sfw
     # MoE grouped: 256 experts, 512 tokens top-8 (~16 rows/expert), K = 6144, N = 4096
     E, N, K = 256, 4096, 6144
@@ -413,8 +437,8 @@ def run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak):
     y = torch.empty((Mt, N), dtype=torch.bfloat16, device=dev)
     ws_bytes = m.nvfp4_grouped_gemm_workspace_bytes(E, Mt, N, K)
     wsp = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    ms = time_launches(lambda i: m.nvfp4_grouped_gemm(qa, sfa, ga, qb, sfb, gb, off_d, E, Mt, N, K,
-                                                      y=y, workspace=wsp), 30, stream)
+    ms = time_graph(lambda i: m.nvfp4_grouped_gemm(qa, sfa, ga, qb, sfb, gb, off_d, E, Mt, N, K,
+                                                   y=y, workspace=wsp), 4, 5, stream)
     hit = int((np.diff(off) > 0).sum())
     mbytes = hit * (N * K // 2 + sfb_bytes)
     gbs = mbytes / (ms * 1e-3) / 1e9
@@ -434,8 +458,8 @@ def run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak):
     aws = torch.empty(m.nvfp4_amax_workspace_bytes(Mp * Kp), dtype=torch.uint8, device=dev)
     yp = torch.empty((Mp, Np), dtype=torch.bfloat16, device=dev)
     m.nvfp4_amax(x, amax, g, aws)
-    ms_q = time_launches(lambda i: m.nvfp4_quantize(x, g, q, sf), 50, stream)
-    ms_amax = time_launches(lambda i: m.nvfp4_amax(x, amax, g, aws), 50, stream)
+    ms_q = time_graph(lambda i: m.nvfp4_quantize(x, g, q, sf), 10, 10, stream)
+    ms_amax = time_graph(lambda i: m.nvfp4_amax(x, amax, g, aws), 10, 10, stream)
     ms_g = time_launches(lambda i: m.nvfp4_gemm(q, sf, g, wcopies[i % 2][0], wcopies[i % 2][1], gw,
                                                 Mp, Np, Kp, y=yp), 20, stream)
 

@@ -150,6 +150,8 @@ int nvfp4_encode_e4m3(const float* v, int64_t n, uint8_t* out, void* stream);
  *   NVFP4_TUNE_STREAM_STAGES   pipeline depth of the streaming kernel (2..16)
  *   NVFP4_TUNE_GROUPED_GRID    persistent CTAs of the grouped kernel
  *   NVFP4_TUNE_GROUPED_STAGES  pipeline depth of the grouped kernel (2..16)
+ *   NVFP4_TUNE_DENSE_KERNEL    large-M kernel: 1 single-CTA 128 x BN tiles, 2 CTA-pair
+ *                              256 x 256 tiles (the default)
  * Returns NVFP4_OK or NVFP4_ERR_INVALID_ARG.
  */
 enum {
@@ -159,7 +161,8 @@ enum {
   NVFP4_TUNE_STREAM_SPLIT = 4,
   NVFP4_TUNE_STREAM_STAGES = 5,
   NVFP4_TUNE_GROUPED_GRID = 6,
-  NVFP4_TUNE_GROUPED_STAGES = 7
+  NVFP4_TUNE_GROUPED_STAGES = 7,
+  NVFP4_TUNE_DENSE_KERNEL = 8
 };
 int nvfp4_tune(int key, int value);
 

@@ -13,6 +13,27 @@
 
 using namespace nvfp4;
 
+cudaError_t nvfp4::allow_max_smem(const void* func) {
+  static std::mutex mu;
+  static const void* seen_fn[64];
+  static int seen_dev[64];
+  static int n_seen = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  for (int i = 0; i < n_seen; ++i)
+    if (seen_fn[i] == func && seen_dev[i] == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  if (e != cudaSuccess) return e;
+  if (n_seen < 64) {
+    seen_fn[n_seen] = func;
+    seen_dev[n_seen] = dev;
+    ++n_seen;
+  }
+  return cudaSuccess;
+}
+
 namespace {
 
 constexpr int kAmaxPartials = 1024;
@@ -23,7 +44,7 @@ thread_local int g_last_launches = 0;
 
 struct Tune {
   int dense_bn = 0, dense_grid = 0, stream_max_m = 0, stream_split = 0, stream_stages = 0, grouped_grid = 0,
-      grouped_stages = 0;
+      grouped_stages = 0, dense_kernel = 0, pair_sfb_half = 0;
 } g_tune;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -80,6 +101,21 @@ int encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+// Scale tensor viewed as [chunks][128] uint32 (one 512-byte tile per row); boxes of
+// four consecutive tiles (the scales of one 256-element K block of 128 rows).
+int encode_sf(CUtensorMap* m, const void* base, uint64_t chunks) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return NVFP4_ERR_CUDA;
+  cuuint64_t dims[2] = {128, chunks};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {128, 4};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
@@ -151,6 +187,13 @@ int nvfp4_tune(int key, int value) {
     case NVFP4_TUNE_GROUPED_STAGES:
       if (value != 0 && (value < 2 || value > 16)) return NVFP4_ERR_INVALID_ARG;
       g_tune.grouped_stages = value;
+      return NVFP4_OK;
+    case NVFP4_TUNE_DENSE_KERNEL:
+      if (value < 0 || value > 2) return NVFP4_ERR_INVALID_ARG;
+      g_tune.dense_kernel = value;
+      return NVFP4_OK;
+    case 9:
+      g_tune.pair_sfb_half = value;
       return NVFP4_OK;
     default:
       return NVFP4_ERR_INVALID_ARG;
@@ -289,6 +332,23 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
     return rc;
   }
 
+  const int kernel = g_tune.dense_kernel ? g_tune.dense_kernel : 2;
+  if (kernel == 2) {
+    // CTA pairs, 256 x 256 tiles
+    CUtensorMap tmA, tmB, tmSFA, tmSFB;
+    if ((rc = encode_2d(&tmA, a, M, K / 2, 128))) return rc;
+    if ((rc = encode_2d(&tmB, b, N, K / 2, 128))) return rc;
+    if ((rc = encode_sf(&tmSFA, sfa, nvfp4_scale_bytes(M, K) / 512))) return rc;
+    if ((rc = encode_sf(&tmSFB, sfb, nvfp4_scale_bytes(N, K) / 512))) return rc;
+    DenseArgs da = {sfa, sfb, ga, gb, y, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), dev_status};
+    const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    int pairs = (g_tune.dense_grid ? g_tune.dense_grid : d.sms) / 2;
+    if (pairs > tiles) pairs = static_cast<int>(tiles);
+    if (pairs < 1) pairs = 1;
+    rc = from_cuda(launch_dense_pair(tmA, tmB, tmSFA, tmSFB, da, 2 * pairs, g_tune.pair_sfb_half == 0, st));
+    g_last_launches = 1;
+    return rc;
+  }
   int bn = g_tune.dense_bn ? g_tune.dense_bn : (N <= 128 ? 128 : 256);
   CUtensorMap tmA, tmB;
   if ((rc = encode_2d(&tmA, a, M, K / 2, 128))) return rc;

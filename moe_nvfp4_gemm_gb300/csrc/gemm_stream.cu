@@ -368,7 +368,7 @@ static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tm
                                    cudaStream_t st) {
   const StreamLayout L(a.x_rows);
   const int smem = a.stages * L.stage_bytes + 1024 + 512;
-  cudaError_t e = cudaFuncSetAttribute(k_gemm_stream<GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_gemm_stream<GROUPED>));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -403,7 +403,7 @@ cudaError_t launch_grouped_prep(const int32_t* offsets, int E, int M_total, int 
                                 cudaStream_t st) {
   const int smem = 2 * (E + 1) * 4;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k_grouped_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_grouped_prep));
     if (e != cudaSuccess) return e;
   }
   k_grouped_prep<<<grid, 256, smem, st>>>(offsets, E, M_total, K, sfx, n_tiles, tiles, slabs, status);

@@ -46,11 +46,18 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t M, int64_t K, const float
 cudaError_t launch_encode(int which, const float* v, int64_t n, uint8_t* out, cudaStream_t st);
 cudaError_t launch_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const DenseArgs& a, int bn, int grid,
                          cudaStream_t st);
+cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
+                              const CUtensorMap& tmSFB, const DenseArgs& a, int grid, bool sfb_full,
+                              cudaStream_t st);
 cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, bool grouped,
                           int grid, cudaStream_t st);
 cudaError_t launch_grouped_prep(const int32_t* offsets, int E, int M_total, int K, const uint8_t* sfx,
                                 int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
                                 cudaStream_t st);
 int stream_smem_bytes(int stages, int x_rows);
+
+// Raises `func`'s dynamic shared-memory limit to the opt-in maximum, once per
+// (kernel, device); later calls only look the pair up.
+cudaError_t allow_max_smem(const void* func);
 
 }  // namespace nvfp4

@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(autouse=True)
 def _reset_tuning():
     yield
-    for key in range(1, 8):
+    for key in range(1, 9):
         m.nvfp4_tune(key, 0)
 
 
@@ -37,21 +37,28 @@ def test_tiny_workload_both_kernels():
     check_gemm(_run(A, B), A, B)
 
 
-@pytest.mark.parametrize("bn", [128, 256])
+TILE_KERNELS = [(1, 128), (1, 256), (2, 0)]  # (single-CTA, BN) and the CTA-pair 256 x 256 kernel
+
+
+@pytest.mark.parametrize("kernel,bn", TILE_KERNELS)
 @pytest.mark.parametrize("M,N,K", [
-    (256, 256, 256), (300, 264, 320), (129, 512, 1024), (1000, 136, 576), (384, 768, 2048)])
-def test_tile_kernel_shapes(bn, M, N, K):
+    (256, 256, 256), (300, 264, 320), (129, 512, 1024), (1000, 136, 576), (384, 768, 2048),
+    (520, 1032, 1344)])
+def test_tile_kernel_shapes(kernel, bn, M, N, K):
     A, B = dense_case(M, N, K, 11, 1.0, 1e-3, 0.02)
     m.nvfp4_tune(m.NVFP4_TUNE_STREAM_MAX_M, -1)
+    m.nvfp4_tune(m.NVFP4_TUNE_DENSE_KERNEL, kernel)
     m.nvfp4_tune(m.NVFP4_TUNE_DENSE_BN, bn)
     check_gemm(_run(A, B), A, B)
 
 
-def test_tile_kernel_persistent_loop_small_grid():
+@pytest.mark.parametrize("kernel,grid", [(1, 3), (2, 6)])
+def test_tile_kernel_persistent_loop_small_grid(kernel, grid):
     # fewer CTAs than tiles: every CTA walks several tiles through the TMEM handoff
     A, B = dense_case(640, 1024, 512, 12, 1.0, 1e-3, 0.02)
     m.nvfp4_tune(m.NVFP4_TUNE_STREAM_MAX_M, -1)
-    m.nvfp4_tune(m.NVFP4_TUNE_DENSE_GRID, 3)
+    m.nvfp4_tune(m.NVFP4_TUNE_DENSE_KERNEL, kernel)
+    m.nvfp4_tune(m.NVFP4_TUNE_DENSE_GRID, grid)
     check_gemm(_run(A, B), A, B)
 
 
@@ -71,8 +78,9 @@ def test_identity_gives_exact_weights():
     codes[np.arange(M), np.arange(M)] = 0x2
     A = Operand(synth.f32_to_bf16_bits(np.eye(M, K, dtype=np.float32)))
     B = Operand(synth.normal_bf16((N, K), 5, 0.02))
-    for max_m in (-1, 128):
+    for max_m, kernel in ((-1, 1), (-1, 2), (128, 0)):
         m.nvfp4_tune(m.NVFP4_TUNE_STREAM_MAX_M, max_m)
+        m.nvfp4_tune(m.NVFP4_TUNE_DENSE_KERNEL, kernel)
         y = _run(A, B)
         ref, _ = oracle.gemm(A.q, A.sf, A.g, B.q, B.sf, B.g, M, N, K)
         ref_bf16 = synth.f32_to_bf16_bits(ref.astype(np.float32))
