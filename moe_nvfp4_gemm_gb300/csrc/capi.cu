@@ -44,7 +44,7 @@ thread_local int g_last_launches = 0;
 
 struct Tune {
   int dense_bn = 0, dense_grid = 0, stream_max_m = 0, stream_split = 0, stream_stages = 0, grouped_grid = 0,
-      grouped_stages = 0, dense_kernel = 0, pair_sfb_half = 0;
+      grouped_stages = 0, dense_kernel = 0;
 } g_tune;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -192,9 +192,7 @@ int nvfp4_tune(int key, int value) {
       if (value < 0 || value > 2) return NVFP4_ERR_INVALID_ARG;
       g_tune.dense_kernel = value;
       return NVFP4_OK;
-    case 9:
-      g_tune.pair_sfb_half = value;
-      return NVFP4_OK;
+
     default:
       return NVFP4_ERR_INVALID_ARG;
   }
@@ -304,7 +302,7 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
     s.N = static_cast<int>(N);
     s.K = static_cast<int>(K);
     s.x_rows = static_cast<int>(pad16(M));
-    s.acc_cols = s.x_rows < 32 ? 32 : s.x_rows;
+    s.acc_cols = (s.x_rows + 31) / 32 * 32;  // the epilogue reads 32-column chunks
     s.acc_bufs = 1;
     int split = g_tune.stream_split;
     if (split == 0) {
@@ -345,7 +343,7 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
     int pairs = (g_tune.dense_grid ? g_tune.dense_grid : d.sms) / 2;
     if (pairs > tiles) pairs = static_cast<int>(tiles);
     if (pairs < 1) pairs = 1;
-    rc = from_cuda(launch_dense_pair(tmA, tmB, tmSFA, tmSFB, da, 2 * pairs, g_tune.pair_sfb_half == 0, st));
+    rc = from_cuda(launch_dense_pair(tmA, tmB, tmSFA, tmSFB, da, 2 * pairs, st));
     g_last_launches = 1;
     return rc;
   }

@@ -3,15 +3,24 @@
 // Operation: "NVFP4 linear layer" (kernelindex, operation header): y = x @ W^T,
 // both operands FP4 with FP8 E4M3FN scales per 16 elements.
 //
-// Persistent warp-specialised tcgen05 kernel, one CTA per SM, tile 128 x BN:
+// Two persistent, warp-specialised tcgen05 kernels share one structure:
 //   warp 0      TMA producer: K-major 128-byte-swizzled data tiles (256 K per
-//               stage) and the matching 512-byte scale tiles (plain bulk copies)
-//               into a STAGES-deep shared-memory ring;
-//   warp 1      allocates TMEM; one lane copies the stage's scales into TMEM
-//               (tcgen05.cp) and issues 4 block-scaled MMAs (K = 64 each),
-//               accumulating in TMEM;
-//   warps 2-5   epilogue: TMEM -> registers, scale by g_a * g_b, bf16, store.
+//               stage) and the matching 512-byte scale tiles into a STAGES-deep
+//               shared-memory ring;
+//   warp 1      allocates TMEM; copies each stage's scales into TMEM (tcgen05.cp)
+//               and issues 4 block-scaled MMAs (K = 64 each) into the accumulator;
+//   warps 2-9   epilogue: each warp drains one TMEM lane quarter and half of the
+//               tile's columns into registers, releases the accumulator, then
+//               scales by g_a * g_b, converts to bf16 and stores.
+// Warps issue TMA and tcgen05 operations converged, through one elected lane.
 // Every wait is bounded (globaltimer watchdog) and reports a timeout status.
+//
+//   k_gemm_dense       one CTA per SM, 128 x BN tiles (tcgen05 cta_group::1)
+//   k_gemm_dense_pair  CTA pairs, 256 x 256 tiles (cta_group::2): each CTA loads
+//                      its 128 rows of A and of B, the even CTA issues the MMAs
+//                      for both SMs (which read B from both CTAs' shared memory);
+//                      per SM this halves the operand traffic per FLOP and makes
+//                      the scale copies free. The default large-M kernel.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -20,6 +29,7 @@
 
 namespace nvfp4 {
 
+constexpr int kDenseThreads = 320;  // producer, MMA, 8 epilogue warps
 
 template <int BN, int STAGES>
 struct DenseCfg {
@@ -37,7 +47,7 @@ struct DenseCfg {
 };
 
 template <int BN, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kDenseThreads, 1)
     k_gemm_dense(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const DenseArgs p) {
   using C = DenseCfg<BN, STAGES>;
@@ -58,7 +68,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, 128);
+    mbar_init(tempty, 8);  // one elected lane per epilogue warp
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -81,16 +91,16 @@ __global__ void __launch_bounds__(192, 1)
   const int n_rowblk = (N + 127) / 128;
 
   if (warp == 0) {
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_last();
-      int s = 0;
-      uint32_t ph = 0;
-      int issued_phase[STAGES];
-      for (int i = 0; i < STAGES; ++i) issued_phase[i] = -1;
-      for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
-        const int m_blk = t % mt, n_blk = t / mt;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) break;
+    const uint64_t pol = policy_evict_last();
+    int s = 0;
+    uint32_t ph = 0;
+    int issued_phase[STAGES];
+    for (int i = 0; i < STAGES; ++i) issued_phase[i] = -1;
+    for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+      const int m_blk = t % mt, n_blk = t / mt;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag)) break;
+        if (elect_one()) {
           const int nsub = min(4, (K - kb * 256) / 64);
           uint8_t* st = smem + s * C::STAGE_BYTES;
           int ngroups = 0;
@@ -107,32 +117,32 @@ __global__ void __launch_bounds__(192, 1)
               bulk_load(st + C::A_BYTES + C::B_BYTES + C::SFA_BYTES + g * 2048, p.sfb + (rb * KC4 + kb * 4) * 512,
                         nsub * 512, &full[s], pol);
           }
-          issued_phase[s] = ph;
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1;
-          }
+        }
+        __syncwarp();
+        issued_phase[s] = ph;
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1;
         }
       }
-      // Let every copy this CTA started land before shared memory is released.
-      for (int i = 0; i < STAGES; ++i)
-        if (issued_phase[i] >= 0) {
-          volatile int32_t dummy = 0;
-          mbar_wait(&full[i], issued_phase[i], &dummy);
-        }
     }
-    __syncwarp();
+    // Let every copy this CTA started land before shared memory is released.
+    for (int i = 0; i < STAGES; ++i)
+      if (issued_phase[i] >= 0) {
+        volatile int32_t dummy = 0;
+        mbar_wait_warp(&full[i], issued_phase[i], &dummy);
+      }
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = idesc_nvf4(128, BN);
-      int s = 0;
-      uint32_t ph = 0, acc_ph = 0;
-      for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
-        if (!mbar_wait(tempty, acc_ph ^ 1, abort_flag)) break;
+    const uint32_t idesc = idesc_nvf4(128, BN);
+    int s = 0;
+    uint32_t ph = 0, acc_ph = 0;
+    for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+      if (!mbar_wait_warp(tempty, acc_ph ^ 1, abort_flag)) break;
+      tc_fence_after();
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait_warp(&full[s], ph, abort_flag)) break;
         tc_fence_after();
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&full[s], ph, abort_flag)) break;
-          tc_fence_after();
+        if (elect_one()) {
           const int nsub = min(4, (K - kb * 256) / 64);
           const uint32_t a_addr = smem_u32(smem + s * C::STAGE_BYTES);
           const uint32_t b_addr = a_addr + C::A_BYTES;
@@ -150,55 +160,38 @@ __global__ void __launch_bounds__(192, 1)
             tc_mma_nvf4(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, sf_col + kk * 4,
                         sf_col + 16 + kk * 4 * C::GROUPS, (kb | kk) != 0);
           tc_commit(&empty[s]);
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1;
-          }
         }
-        tc_commit(tfull);
-        acc_ph ^= 1;
+        __syncwarp();
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1;
+        }
       }
-      // All MMAs issued by this thread complete before TMEM is released.
-      tc_commit(drain);
-      volatile int32_t dummy = 0;
-      mbar_wait(drain, 0, &dummy);
+      if (elect_one()) tc_commit(tfull);
+      __syncwarp();
+      acc_ph ^= 1;
     }
+    // All MMAs issued by this warp complete before TMEM is released.
+    if (elect_one()) tc_commit(drain);
     __syncwarp();
+    volatile int32_t dummy = 0;
+    mbar_wait_warp(drain, 0, &dummy);
   } else {
-    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    const int q = warp & 3;         // TMEM lane quarter this warp may read
+    const int h = (warp - 2) >> 2;  // which half of the tile's columns
     const float alpha = __ldg(p.ga) * __ldg(p.gb);
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
       const int m_blk = t % mt, n_blk = t / mt;
-      if (!mbar_wait(tfull, acc_ph, abort_flag)) break;
+      if (!mbar_wait_warp(tfull, acc_ph, abort_flag)) break;
       tc_fence_after();
       const int row = m_blk * 128 + q * 32 + lane;
-      uint16_t* yrow = p.y + static_cast<int64_t>(row) * N;
-#pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t r0[16], r1[16];
-        const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + c;
-        tmem_ld16(ta, r0);
-        tmem_ld16(ta + 16, r1);
-        tmem_ld_wait();
-        const int col = n_blk * BN + c;
-        if (row < M) {
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int cc = col + h * 8;
-            if (cc < N) {
-              const uint32_t* r = (h < 2) ? r0 : r1;
-              const int o = (h & 1) * 8;
-              st_global_v4(yrow + cc, pack_bf16x2(__uint_as_float(r[o + 0]) * alpha, __uint_as_float(r[o + 1]) * alpha),
-                           pack_bf16x2(__uint_as_float(r[o + 2]) * alpha, __uint_as_float(r[o + 3]) * alpha),
-                           pack_bf16x2(__uint_as_float(r[o + 4]) * alpha, __uint_as_float(r[o + 5]) * alpha),
-                           pack_bf16x2(__uint_as_float(r[o + 6]) * alpha, __uint_as_float(r[o + 7]) * alpha));
-            }
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(tempty);
+      drain_accumulator<BN / 2>(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * (BN / 2), alpha,
+                                p.y + static_cast<int64_t>(row) * N, row < M, n_blk * BN + h * (BN / 2), N,
+                                [&] {
+                                  if (elect_one()) mbar_arrive(tempty);
+                                  __syncwarp();
+                                });
       acc_ph ^= 1;
     }
   }
@@ -212,37 +205,27 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0 && *abort_flag) report_status(p.status, kStatusTimeout);
 }
 
-// ---- CTA-pair variant: 256 x 256 tiles on two SMs ---------------------------------------
-//
-// A cluster of two CTAs computes one 256 x 256 tile with tcgen05 cta_group::2: each
-// CTA loads its own 128 rows of A and its own 128 rows of B (the MMA reads B from
-// both CTAs' shared memory) plus the scale tiles, all signalling the even CTA's
-// barriers; one thread of the even CTA issues the scale copies and the MMAs for
-// both SMs, and each CTA's epilogue drains its own 128 x 256 half from its TMEM.
-// Per SM and K = 64 step this moves 8 KB of operands for 4.2 MFLOP, against 12 KB
-// for the single-CTA 128 x 256 tile.
-template <bool SFB_FULL>
+// ---- CTA-pair kernel: 256 x 256 tiles on two SMs -----------------------------------------
+
 struct PairCfg {
   static constexpr int STAGES = 5;
   static constexpr int A_BYTES = 128 * 128;
   static constexpr int B_BYTES = 128 * 128;
   static constexpr int SFA_BYTES = 2048;
-  static constexpr int SFB_BYTES = SFB_FULL ? 4096 : 2048;
+  static constexpr int SFB_BYTES = 4096;  // scales of all 256 B rows, in both CTAs
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int SFB_COLS_PER_K = SFB_FULL ? 8 : 4;
-  static constexpr int SF_COLS = 16 + 4 * SFB_COLS_PER_K;
+  static constexpr int SF_COLS = 16 + 32;
   static constexpr int TMEM_COLS = 512;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
   static_assert(256 + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-template <bool SFB_FULL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kDenseThreads, 1)
     k_gemm_dense_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                       const DenseArgs p) {
-  using C = PairCfg<SFB_FULL>;
+  using C = PairCfg;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -263,7 +246,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, 256);
+    mbar_init(tempty, 16);  // one elected lane per epilogue warp, both CTAs
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -289,127 +272,101 @@ __global__ void __launch_bounds__(192, 1)
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (warp == 0) {
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_last();
-      int s = 0;
-      uint32_t ph = 0;
-      int issued_phase[STAGES];
-      for (int i = 0; i < STAGES; ++i) issued_phase[i] = -1;
-      for (int t = pair; t < tiles && !*abort_flag; t += npairs) {
-        const int m_blk = t % mt, n_blk = t / mt;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) break;
+    const uint64_t pol = policy_evict_last();
+    int s = 0;
+    uint32_t ph = 0;
+    int issued_phase[STAGES];
+    for (int i = 0; i < STAGES; ++i) issued_phase[i] = -1;
+    for (int t = pair; t < tiles && !*abort_flag; t += npairs) {
+      const int m_blk = t % mt, n_blk = t / mt;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag)) break;
+        if (elect_one()) {
           uint8_t* st = smem + s * C::STAGE_BYTES;
           const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
           if (leader) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE_BYTES);
           tma_load_2d_pair(st, &tmA, bar, kb * 128, m_blk * 256 + rank * 128, pol);
           tma_load_2d_pair(st + C::A_BYTES, &tmB, bar, kb * 128, n_blk * 256 + rank * 128, pol);
           tma_load_2d_pair(st + C::A_BYTES + C::B_BYTES, &tmSFA, bar, 0, (m_blk * 2 + rank) * KC4 + kb * 4, pol);
-          if (SFB_FULL) {
-            tma_load_2d_pair(st + C::A_BYTES + C::B_BYTES + C::SFA_BYTES, &tmSFB, bar, 0, (n_blk * 2) * KC4 + kb * 4,
-                             pol);
-            tma_load_2d_pair(st + C::A_BYTES + C::B_BYTES + C::SFA_BYTES + 2048, &tmSFB, bar, 0,
-                             (n_blk * 2 + 1) * KC4 + kb * 4, pol);
-          } else {
-            tma_load_2d_pair(st + C::A_BYTES + C::B_BYTES + C::SFA_BYTES, &tmSFB, bar, 0,
-                             (n_blk * 2 + rank) * KC4 + kb * 4, pol);
-          }
-          issued_phase[s] = ph;
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1;
-          }
+          tma_load_2d_pair(st + C::A_BYTES + C::B_BYTES + C::SFA_BYTES, &tmSFB, bar, 0, (n_blk * 2) * KC4 + kb * 4,
+                           pol);
+          tma_load_2d_pair(st + C::A_BYTES + C::B_BYTES + C::SFA_BYTES + 2048, &tmSFB, bar, 0,
+                           (n_blk * 2 + 1) * KC4 + kb * 4, pol);
+        }
+        __syncwarp();
+        issued_phase[s] = ph;
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1;
         }
       }
-      // The even CTA's full barriers count both CTAs' bytes: let them all land.
-      if (leader)
-        for (int i = 0; i < STAGES; ++i)
-          if (issued_phase[i] >= 0) {
-            volatile int32_t dummy = 0;
-            mbar_wait(&full[i], issued_phase[i], &dummy);
-          }
     }
-    __syncwarp();
+    // The even CTA's full barriers count both CTAs' bytes: let them all land.
+    if (leader)
+      for (int i = 0; i < STAGES; ++i)
+        if (issued_phase[i] >= 0) {
+          volatile int32_t dummy = 0;
+          mbar_wait_warp(&full[i], issued_phase[i], &dummy);
+        }
   } else if (warp == 1) {
-    if (leader && lane == 0) {
+    if (leader) {
       const uint32_t idesc = idesc_nvf4(256, 256);
       int s = 0;
       uint32_t ph = 0, acc_ph = 0;
       for (int t = pair; t < tiles && !*abort_flag; t += npairs) {
-        if (!mbar_wait(tempty, acc_ph ^ 1, abort_flag)) break;
+        if (!mbar_wait_warp(tempty, acc_ph ^ 1, abort_flag)) break;
         tc_fence_after();
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&full[s], ph, abort_flag)) break;
+          if (!mbar_wait_warp(&full[s], ph, abort_flag)) break;
           tc_fence_after();
-          const int nsub = min(4, (K - kb * 256) / 64);
-          const uint32_t a_addr = smem_u32(smem + s * C::STAGE_BYTES);
-          const uint32_t b_addr = a_addr + C::A_BYTES;
-          const uint32_t sfa_addr = b_addr + C::B_BYTES;
-          const uint32_t sfb_addr = sfa_addr + C::SFA_BYTES;
-          const uint32_t sf_col = tmem + 256 + s * C::SF_COLS;
-          for (int kk = 0; kk < nsub; ++kk) {
-            tc_cp_32x128b_x4_pair(sf_col + kk * 4, desc_sf(sfa_addr + kk * 512));
-            if (SFB_FULL) {
+          if (elect_one()) {
+            const int nsub = min(4, (K - kb * 256) / 64);
+            const uint32_t a_addr = smem_u32(smem + s * C::STAGE_BYTES);
+            const uint32_t b_addr = a_addr + C::A_BYTES;
+            const uint32_t sfa_addr = b_addr + C::B_BYTES;
+            const uint32_t sfb_addr = sfa_addr + C::SFA_BYTES;
+            const uint32_t sf_col = tmem + 256 + s * C::SF_COLS;
+            for (int kk = 0; kk < nsub; ++kk) {
+              tc_cp_32x128b_x4_pair(sf_col + kk * 4, desc_sf(sfa_addr + kk * 512));
               tc_cp_32x128b_x4_pair(sf_col + 16 + kk * 8, desc_sf(sfb_addr + kk * 512));
               tc_cp_32x128b_x4_pair(sf_col + 16 + kk * 8 + 4, desc_sf(sfb_addr + 2048 + kk * 512));
-            } else {
-              tc_cp_32x128b_x4_pair(sf_col + 16 + kk * 4, desc_sf(sfb_addr + kk * 512));
             }
+            const uint64_t adesc = desc_sw128(a_addr), bdesc = desc_sw128(b_addr);
+            for (int kk = 0; kk < nsub; ++kk)
+              tc_mma_nvf4_pair(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, sf_col + kk * 4, sf_col + 16 + kk * 8,
+                               (kb | kk) != 0);
+            tc_commit_pair(&empty[s], 3);
           }
-          const uint64_t adesc = desc_sw128(a_addr), bdesc = desc_sw128(b_addr);
-          for (int kk = 0; kk < nsub; ++kk)
-            tc_mma_nvf4_pair(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, sf_col + kk * 4,
-                             sf_col + 16 + kk * C::SFB_COLS_PER_K, (kb | kk) != 0);
-          tc_commit_pair(&empty[s], 3);
+          __syncwarp();
           if (++s == STAGES) {
             s = 0;
             ph ^= 1;
           }
         }
-        tc_commit_pair(tfull, 3);
+        if (elect_one()) tc_commit_pair(tfull, 3);
+        __syncwarp();
         acc_ph ^= 1;
       }
-      tc_commit_pair(drain, 1);
+      if (elect_one()) tc_commit_pair(drain, 1);
+      __syncwarp();
       volatile int32_t dummy = 0;
-      mbar_wait(drain, 0, &dummy);
+      mbar_wait_warp(drain, 0, &dummy);
     }
-    __syncwarp();
   } else {
-    const int q = warp & 3;
+    const int q = warp & 3, h = (warp - 2) >> 2;
     const float alpha = __ldg(p.ga) * __ldg(p.gb);
     const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
     uint32_t acc_ph = 0;
     for (int t = pair; t < tiles; t += npairs) {
       const int m_blk = t % mt, n_blk = t / mt;
-      if (!mbar_wait(tfull, acc_ph, abort_flag)) break;
+      if (!mbar_wait_warp(tfull, acc_ph, abort_flag)) break;
       tc_fence_after();
       const int row = m_blk * 256 + rank * 128 + q * 32 + lane;
-      uint16_t* yrow = p.y + static_cast<int64_t>(row) * N;
-#pragma unroll 1
-      for (int c = 0; c < 256; c += 32) {
-        uint32_t r0[16], r1[16];
-        const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + c;
-        tmem_ld16(ta, r0);
-        tmem_ld16(ta + 16, r1);
-        tmem_ld_wait();
-        const int col = n_blk * 256 + c;
-        if (row < M) {
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int cc = col + h * 8;
-            if (cc < N) {
-              const uint32_t* r = (h < 2) ? r0 : r1;
-              const int o = (h & 1) * 8;
-              st_global_v4(yrow + cc, pack_bf16x2(__uint_as_float(r[o + 0]) * alpha, __uint_as_float(r[o + 1]) * alpha),
-                           pack_bf16x2(__uint_as_float(r[o + 2]) * alpha, __uint_as_float(r[o + 3]) * alpha),
-                           pack_bf16x2(__uint_as_float(r[o + 4]) * alpha, __uint_as_float(r[o + 5]) * alpha),
-                           pack_bf16x2(__uint_as_float(r[o + 6]) * alpha, __uint_as_float(r[o + 7]) * alpha));
-            }
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive_cluster(tempty_leader);
+      drain_accumulator<128>(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128, alpha,
+                             p.y + static_cast<int64_t>(row) * N, row < M, n_blk * 256 + h * 128, N, [&] {
+                               if (elect_one()) mbar_arrive_cluster(tempty_leader);
+                               __syncwarp();
+                             });
       acc_ph ^= 1;
     }
   }
@@ -424,35 +381,7 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0 && *abort_flag) report_status(p.status, kStatusTimeout);
 }
 
-template <bool SFB_FULL>
-static cudaError_t launch_pair_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
-                                 const CUtensorMap& tmSFB, const DenseArgs& a, int grid, cudaStream_t st) {
-  using C = PairCfg<SFB_FULL>;
-  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_gemm_dense_pair<SFB_FULL>));
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k_gemm_dense_pair<SFB_FULL>, tmA, tmB, tmSFA, tmSFB, a);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
-
-// grid: an even number of CTAs (two per 256 x 256 tile in flight).
-cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
-                              const CUtensorMap& tmSFB, const DenseArgs& a, int grid, bool sfb_full, cudaStream_t st) {
-  return sfb_full ? launch_pair_t<true>(tmA, tmB, tmSFA, tmSFB, a, grid, st)
-                  : launch_pair_t<false>(tmA, tmB, tmSFA, tmSFB, a, grid, st);
-}
+// ---- host launchers ---------------------------------------------------------------------------
 
 template <int BN, int STAGES>
 static cudaError_t launch_dense_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const DenseArgs& a, int grid,
@@ -460,7 +389,7 @@ static cudaError_t launch_dense_t(const CUtensorMap& tmA, const CUtensorMap& tmB
   using C = DenseCfg<BN, STAGES>;
   cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_gemm_dense<BN, STAGES>));
   if (e != cudaSuccess) return e;
-  k_gemm_dense<BN, STAGES><<<grid, 192, C::SMEM_BYTES, st>>>(tmA, tmB, a);
+  k_gemm_dense<BN, STAGES><<<grid, kDenseThreads, C::SMEM_BYTES, st>>>(tmA, tmB, a);
   return cudaGetLastError();
 }
 
@@ -469,6 +398,28 @@ cudaError_t launch_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const D
                          cudaStream_t st) {
   if (bn == 256) return launch_dense_t<256, 4>(tmA, tmB, a, grid, st);
   return launch_dense_t<128, 6>(tmA, tmB, a, grid, st);
+}
+
+// grid: an even number of CTAs (two per 256 x 256 tile in flight).
+cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
+                              const CUtensorMap& tmSFB, const DenseArgs& a, int grid, cudaStream_t st) {
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_gemm_dense_pair));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDenseThreads);
+  cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k_gemm_dense_pair, tmA, tmB, tmSFA, tmSFB, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace nvfp4

@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], 4);  // one elected lane per epilogue warp
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -146,20 +146,20 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sf_base = tmem + p.acc_bufs * p.acc_cols;
 
   if (warp == 0) {
-    if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-      int s = 0;
-      uint32_t ph = 0;
-      int issued_phase[16];
-      for (int i = 0; i < 16; ++i) issued_phase[i] = -1;
-      Item it;
-      for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it) && !*abort_flag; i += stride) {
-        const int n16 = (it.rows + 15) >> 4;
-        const int64_t wrow0 = static_cast<int64_t>(it.e) * N + it.wt * 128;
-        const uint8_t* sfw = p.sfw + it.e * p.sfw_stride + static_cast<int64_t>(it.wt) * KC4 * 512;
-        const uint8_t* sfx = p.sfx + static_cast<int64_t>(it.slab) * KC4 * 512;
-        for (int kb = it.kb0; kb < it.kb1; ++kb) {
-          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) break;
+    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+    int s = 0;
+    uint32_t ph = 0;
+    int issued_phase[16];
+    for (int i = 0; i < 16; ++i) issued_phase[i] = -1;
+    Item it;
+    for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it) && !*abort_flag; i += stride) {
+      const int n16 = (it.rows + 15) >> 4;
+      const int64_t wrow0 = static_cast<int64_t>(it.e) * N + it.wt * 128;
+      const uint8_t* sfw = p.sfw + it.e * p.sfw_stride + static_cast<int64_t>(it.wt) * KC4 * 512;
+      const uint8_t* sfx = p.sfx + static_cast<int64_t>(it.slab) * KC4 * 512;
+      for (int kb = it.kb0; kb < it.kb1; ++kb) {
+        if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag)) break;
+        if (elect_one()) {
           const int nsub = min(4, (K - kb * 256) / 64);
           uint8_t* st = smem + s * L.stage_bytes;
           mbar_arrive_expect_tx(&full[s], 16384 + n16 * 2048 + nsub * 1024);
@@ -168,34 +168,34 @@ __global__ void __launch_bounds__(192, 1)
             tma_load_2d(st + L.x_off + j * 2048, &tmX, &full[s], kb * 128, it.row0 + j * 16, pol_x);
           bulk_load(st + L.sfw_off, sfw + kb * 2048, nsub * 512, &full[s], pol_w);
           bulk_load(st + L.sfx_off, sfx + kb * 2048, nsub * 512, &full[s], pol_x);
-          issued_phase[s] = ph;
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1;
-          }
+        }
+        __syncwarp();
+        issued_phase[s] = ph;
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1;
         }
       }
-      for (int i = 0; i < STAGES; ++i)
-        if (issued_phase[i] >= 0) {
-          volatile int32_t dummy = 0;
-          mbar_wait(&full[i], issued_phase[i], &dummy);
-        }
     }
-    __syncwarp();
+    for (int i = 0; i < STAGES; ++i)
+      if (issued_phase[i] >= 0) {
+        volatile int32_t dummy = 0;
+        mbar_wait_warp(&full[i], issued_phase[i], &dummy);
+      }
   } else if (warp == 1) {
-    if (lane == 0) {
-      int s = 0, buf = 0;
-      uint32_t ph = 0, acc_ph[2] = {0, 0};
-      Item it;
-      for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it) && !*abort_flag; i += stride) {
-        const int n_mma = ((it.rows + 15) >> 4) * 16;
-        const uint32_t idesc = idesc_nvf4(128, n_mma);
-        const uint32_t acc = tmem + buf * p.acc_cols;
-        if (!mbar_wait(&tempty[buf], acc_ph[buf] ^ 1, abort_flag)) break;
+    int s = 0, buf = 0;
+    uint32_t ph = 0, acc_ph[2] = {0, 0};
+    Item it;
+    for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it) && !*abort_flag; i += stride) {
+      const int n_mma = ((it.rows + 15) >> 4) * 16;
+      const uint32_t idesc = idesc_nvf4(128, n_mma);
+      const uint32_t acc = tmem + buf * p.acc_cols;
+      if (!mbar_wait_warp(&tempty[buf], acc_ph[buf] ^ 1, abort_flag)) break;
+      tc_fence_after();
+      for (int kb = it.kb0; kb < it.kb1; ++kb) {
+        if (!mbar_wait_warp(&full[s], ph, abort_flag)) break;
         tc_fence_after();
-        for (int kb = it.kb0; kb < it.kb1; ++kb) {
-          if (!mbar_wait(&full[s], ph, abort_flag)) break;
-          tc_fence_after();
+        if (elect_one()) {
           const int nsub = min(4, (K - kb * 256) / 64);
           const uint32_t w_addr = smem_u32(smem + s * L.stage_bytes);
           const uint32_t x_addr = w_addr + L.x_off;
@@ -209,21 +209,24 @@ __global__ void __launch_bounds__(192, 1)
             tc_mma_nvf4(acc, wdesc + 2 * kk, xdesc + 2 * kk, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4,
                         (kb != it.kb0) || (kk != 0));
           tc_commit(&empty[s]);
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1;
-          }
         }
-        tc_commit(&tfull[buf]);
-        acc_ph[buf] ^= 1;
-        buf = (buf + 1 == p.acc_bufs) ? 0 : buf + 1;
+        __syncwarp();
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1;
+        }
       }
-      tc_commit(drain);
-      volatile int32_t dummy = 0;
-      mbar_wait(drain, 0, &dummy);
+      if (elect_one()) tc_commit(&tfull[buf]);
+      __syncwarp();
+      acc_ph[buf] ^= 1;
+      buf = (buf + 1 == p.acc_bufs) ? 0 : buf + 1;
     }
+    if (elect_one()) tc_commit(drain);
     __syncwarp();
+    volatile int32_t dummy = 0;
+    mbar_wait_warp(drain, 0, &dummy);
   } else {
+    constexpr int MAXC = GROUPED ? kGroupTile : 128;
     const int q = warp & 3;
     const float ga = __ldg(p.ga);
     int buf = 0;
@@ -231,33 +234,33 @@ __global__ void __launch_bounds__(192, 1)
     float* red = reinterpret_cast<float*>(smem);  // split-K partials (stage memory, reused)
     Item it;
     for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it); i += stride) {
-      if (!mbar_wait(&tfull[buf], acc_ph[buf], abort_flag)) break;
+      if (!mbar_wait_warp(&tfull[buf], acc_ph[buf], abort_flag)) break;
       tc_fence_after();
       const float alpha = ga * __ldg(p.gb + it.e);
       const int wrow = it.wt * 128 + q * 32 + lane;  // output column
       const int n_mma = ((it.rows + 15) >> 4) * 16;
       const bool has_k = it.kb1 > it.kb0;
-      for (int c = 0; c < n_mma; c += 16) {
-        uint32_t r[16];
-        tmem_ld16(tmem + buf * p.acc_cols + (static_cast<uint32_t>(q * 32) << 16) + c, r);
-        tmem_ld_wait();
-        if (!GROUPED && p.split > 1) {
+      // all of this item's columns into registers, then release the accumulator
+      uint32_t r[MAXC];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) red[(c + j) * 128 + q * 32 + lane] = has_k ? __uint_as_float(r[j]) : 0.0f;
-        } else if (wrow < N) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int tok = c + j;
-            if (tok < it.rows) {
-              const float v = __uint_as_float(r[j]) * alpha;
-              p.y[static_cast<int64_t>(it.row0 + tok) * N + wrow] =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(v));
-            }
-          }
-        }
-      }
+      for (int c = 0; c < MAXC; c += 32)
+        if (c < n_mma) tmem_ld32(tmem + buf * p.acc_cols + (static_cast<uint32_t>(q * 32) << 16) + c, r + c);
+      tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&tempty[buf]);
+      __syncwarp();
+      if (elect_one()) mbar_arrive(&tempty[buf]);
+      __syncwarp();
+      if (!GROUPED && p.split > 1) {
+#pragma unroll
+        for (int j = 0; j < MAXC; ++j)
+          if (j < n_mma) red[j * 128 + q * 32 + lane] = has_k ? __uint_as_float(r[j]) : 0.0f;
+      } else if (wrow < N) {
+#pragma unroll
+        for (int j = 0; j < MAXC; ++j)
+          if (j < it.rows)
+            p.y[static_cast<int64_t>(it.row0 + j) * N + wrow] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j]) * alpha));
+      }
       acc_ph[buf] ^= 1;
       buf = (buf + 1 == p.acc_bufs) ? 0 : buf + 1;
     }

@@ -25,7 +25,17 @@ DEVI uint64_t globaltimer_ns() {
   return t;
 }
 
-DEVI bool elect_lane0() { return (threadIdx.x & 31) == 0; }
+// One lane of a converged warp (elect.sync). Issuing tcgen05 and TMA operations
+// from a converged warp through an elected lane keeps their operands warp-uniform.
+DEVI bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
 
 // ---- mbarrier ---------------------------------------------------------------
 
@@ -73,6 +83,11 @@ DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
       return false;
     }
   }
+}
+
+// Warp-collective wait: every lane polls, the result is the same in all lanes.
+DEVI bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort)) != 0;
 }
 
 // ---- TMA ----------------------------------------------------------------------
@@ -200,6 +215,19 @@ DEVI void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+// 32 lanes x 32 consecutive 32-bit columns.
+DEVI void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
 DEVI void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // CTA-pair forms: allocation by one warp of each CTA of the pair; MMA, scale copy
@@ -280,6 +308,32 @@ DEVI uint32_t pack_bf16x2(float lo, float hi) {
 DEVI void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
+}
+
+// Drains NC accumulator columns (one TMEM lane quarter, starting at taddr) of one
+// warp into registers, releases the accumulator through `release` (called by the
+// whole warp after the loads completed), then scales by alpha and stores bf16
+// to yrow[col0 .. col0 + NC) (columns >= N skipped, in groups of 8).
+template <int NC, typename Release>
+DEVI void drain_accumulator(uint32_t taddr, float alpha, uint16_t* yrow, bool row_ok, int col0, int N,
+                            Release release) {
+  uint32_t r[NC];
+#pragma unroll
+  for (int c = 0; c < NC; c += 32) tmem_ld32(taddr + c, r + c);
+  tmem_ld_wait();
+  tc_fence_before();
+  __syncwarp();
+  release();
+  if (row_ok) {
+#pragma unroll
+    for (int c = 0; c < NC; c += 8) {
+      if (col0 + c < N)
+        st_global_v4(yrow + col0 + c, pack_bf16x2(__uint_as_float(r[c + 0]) * alpha, __uint_as_float(r[c + 1]) * alpha),
+                     pack_bf16x2(__uint_as_float(r[c + 2]) * alpha, __uint_as_float(r[c + 3]) * alpha),
+                     pack_bf16x2(__uint_as_float(r[c + 4]) * alpha, __uint_as_float(r[c + 5]) * alpha),
+                     pack_bf16x2(__uint_as_float(r[c + 6]) * alpha, __uint_as_float(r[c + 7]) * alpha));
+    }
+  }
 }
 
 DEVI void report_status(int32_t* status, int32_t code) {
