@@ -130,6 +130,35 @@ int nvfp4_grouped_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, co
                        size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * Allocation-free variant of nvfp4_grouped_gemm. The pages have no counterpart;
+ * it exists for callers that cannot call cudaMalloc at the point where they run
+ * the MoE layer: code that runs while a stream is being captured into a CUDA
+ * graph, runtimes that give kernels a fixed memory budget and no allocator, and
+ * plugins that must not reach into the host program's allocator.
+ *
+ * Same arguments and result as nvfp4_grouped_gemm, minus the workspace: the
+ * scratch (tile list and per-tile activation scales) lives in one array of
+ * NVFP4_NOALLOC_SCRATCH_BYTES (16 MiB) compiled into the library, present on
+ * every device that loads the library until the process exits.
+ *   - Returns NVFP4_ERR_WORKSPACE when nvfp4_grouped_gemm_workspace_bytes(E,
+ *     M_total, N, K) exceeds NVFP4_NOALLOC_SCRATCH_BYTES (256 experts with 4096
+ *     routed rows and K = 6144 need 15.0 MiB and fit).
+ *   - The first call on a device looks up the array's device address with that
+ *     device current (cudaGetSymbolAddress); make that first call before any
+ *     stream capture. Later calls do no CUDA call besides the launches.
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents. The kernels write every scratch byte they read, so nothing needs
+ *     clearing between calls, but calls that overlap on the GPU (unordered streams)
+ *     race on it: order them.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define NVFP4_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int nvfp4_grouped_gemm_noalloc(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b,
+                               const uint8_t* sfb, const float* gb, const int32_t* expert_offsets, int32_t E,
+                               int64_t M_total, int64_t N, int64_t K, uint16_t* y, int32_t* dev_status,
+                               void* stream);
+
+/*
  * Elementwise device encoders used by the quantiser, for exhaustive checks:
  * fp32 -> E2M1 code (round to nearest even, saturating, sign kept) and
  * fp32 -> E4M3FN code (round to nearest even, saturating to +-448).

@@ -32,7 +32,8 @@ STATUS = {0: "NVFP4_OK", -1: "NVFP4_ERR_INVALID_ARG", -2: "NVFP4_ERR_UNSUPPORTED
 
 EXPORTS = ["nvfp4_status_string", "nvfp4_scale_bytes", "nvfp4_amax_workspace_bytes", "nvfp4_amax",
            "nvfp4_quantize", "nvfp4_gemm_workspace_bytes", "nvfp4_gemm",
-           "nvfp4_grouped_gemm_workspace_bytes", "nvfp4_grouped_gemm", "nvfp4_encode_e2m1",
+           "nvfp4_grouped_gemm_workspace_bytes", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_noalloc",
+           "nvfp4_encode_e2m1",
            "nvfp4_encode_e4m3", "nvfp4_tune", "nvfp4_last_launch_count"]
 
 
@@ -76,6 +77,8 @@ def lib():
             L.nvfp4_grouped_gemm_workspace_bytes.argtypes = [_i32, _i64, _i64, _i64]
             L.nvfp4_grouped_gemm.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64,
                                              _i64, _vp, _vp, _sz, _vp, _vp]
+            L.nvfp4_grouped_gemm_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64,
+                                                     _i64, _i64, _vp, _vp, _vp]
             L.nvfp4_encode_e2m1.argtypes = [_vp, _i64, _vp, _vp]
             L.nvfp4_encode_e4m3.argtypes = [_vp, _i64, _vp, _vp]
             L.nvfp4_tune.argtypes = [ctypes.c_int, ctypes.c_int]
@@ -192,6 +195,29 @@ def nvfp4_grouped_gemm(a, sfa, ga, b, sfb, gb, expert_offsets, E: int, M_total: 
                                     _ptr(expert_offsets), E, M_total, N, K, _ptr(y),
                                     _ptr(workspace), workspace.numel(), _ptr(dev_status),
                                     _stream(stream)))
+    return y
+
+
+NVFP4_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+
+
+def nvfp4_grouped_gemm_noalloc(a, sfa, ga, b, sfb, gb, expert_offsets, E: int, M_total: int, N: int,
+                               K: int, y=None, dev_status=None, stream=None):
+    """nvfp4_grouped_gemm without a workspace argument: the library's built-in scratch is used.
+
+    For callers that cannot allocate device memory where they run the MoE layer (for
+    example inside CUDA-graph capture). Only `y` is allocated here when not given.
+    """
+    for t, n in ((a, "a"), (sfa, "sfa"), (b, "b"), (sfb, "sfb")):
+        _cuda(t, torch.uint8, n)
+    _cuda(ga, torch.float32, "ga")
+    _cuda(gb, torch.float32, "gb")
+    _cuda(expert_offsets, torch.int32, "expert_offsets")
+    y = torch.empty((M_total, N), dtype=torch.bfloat16, device=a.device) if y is None else y
+    _check("nvfp4_grouped_gemm_noalloc",
+           lib().nvfp4_grouped_gemm_noalloc(_ptr(a), _ptr(sfa), _ptr(ga), _ptr(b), _ptr(sfb), _ptr(gb),
+                                            _ptr(expert_offsets), E, M_total, N, K, _ptr(y),
+                                            _ptr(dev_status), _stream(stream)))
     return y
 
 

@@ -442,3 +442,39 @@ int nvfp4_grouped_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, co
 }
 
 }  // extern "C"
+
+// ---- allocation-free grouped GEMM ------------------------------------------------------------
+
+// Scratch of nvfp4_grouped_gemm_noalloc: one copy on every device that loads this
+// library, held until the process exits. In host code this name is only a stand-in;
+// the device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) uint8_t g_grouped_scratch[NVFP4_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_dev_ptr[64];  // per device: device address of g_grouped_scratch, or null
+}  // namespace
+
+extern "C" int nvfp4_grouped_gemm_noalloc(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b,
+                                          const uint8_t* sfb, const float* gb, const int32_t* expert_offsets,
+                                          int32_t E, int64_t M_total, int64_t N, int64_t K, uint16_t* y,
+                                          int32_t* dev_status, void* stream) {
+  g_last_launches = 0;
+  if (nvfp4_grouped_gemm_workspace_bytes(E, M_total, N, K) > NVFP4_NOALLOC_SCRATCH_BYTES)
+    return NVFP4_ERR_WORKSPACE;  // problem too large for the fixed scratch
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NVFP4_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_dev_ptr[dev]) {
+      // first call on this device (which is current): look the array's address up once
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_grouped_scratch) != cudaSuccess || !ptr) return NVFP4_ERR_CUDA;
+      g_scratch_dev_ptr[dev] = ptr;
+    }
+    scratch = g_scratch_dev_ptr[dev];
+  }
+  return nvfp4_grouped_gemm(a, sfa, ga, b, sfb, gb, expert_offsets, E, M_total, N, K, y, scratch,
+                            NVFP4_NOALLOC_SCRATCH_BYTES, dev_status, stream);
+}
