@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-breakdown", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--only", choices=["decode", "moe", "prefill"], default=None,
+                    help="run only this breakdown workload (for profiling) and print its numbers")
     return ap.parse_args()
 
 
@@ -244,6 +246,25 @@ def main():
     import synth
 
     dev = torch.device("cuda", local)
+    if args.only:
+        stream = torch.cuda.current_stream()
+        peaks = load_peaks()
+
+        def to_dev_only(a):
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+            return torch.from_numpy(a).to(dev)
+
+        def quantize_only(bf16_dev):
+            amax, g = m.nvfp4_amax(bf16_dev)
+            q, sf = m.nvfp4_quantize(bf16_dev, g)
+            return q, sf, g
+
+        out = run_breakdown(m, synth, dev, stream, to_dev_only, quantize_only, peaks,
+                            peaks["bf16"] * FP4_OVER_BF16, only=args.only)
+        print(json.dumps({"only": args.only, "breakdown": out}), flush=True)
+        return
     stream = torch.cuda.current_stream()
     peaks = load_peaks()
     fp4_peak = peaks["bf16"] * FP4_OVER_BF16  # TFLOP/s
@@ -403,10 +424,21 @@ def time_graph(fn, calls, reps, stream):
     return a.elapsed_time(b) / (calls * reps)
 
 
-def run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak):
+def run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak, only=None):
     import torch
     out = {}
     hbm = peaks["hbm"]
+    if only in (None, "decode"):
+        run_decode(m, synth, dev, stream, to_dev, quantize_dev, hbm, out)
+    if only in (None, "moe"):
+        run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out)
+    if only in (None, "prefill"):
+        run_prefill(m, synth, dev, stream, to_dev, quantize_dev, hbm, fp4_peak, out)
+    return out
+
+
+def run_decode(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
+    import torch
     # decode: M in {1, 16, 32}, N = K = 8192; 8 rotating weight copies (302 MB > L2)
     w = synth.normal_bf16((SQ, SQ), 2 * 2 + 1, 0.02)
     wq, sfw, gw = quantize_dev(to_dev(w))
@@ -425,6 +457,10 @@ def run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak):
                                "bytes": wbytes, "timing": "CUDA graph of 16 calls over 8 weight copies",
                                "us_eager_per_launch_events": ms_eager * 1e3}
     del copies, wq, sfw
+
+
+def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
+    import torch
     # MoE grouped: 256 experts, 512 tokens top-8 (~16 rows/expert), K = 6144, N = 4096
     E, N, K = 256, 4096, 6144
     a_rows, off, tok = synth.moe_tokens(512, E, 8, K, 3)
@@ -452,6 +488,10 @@ def run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak):
                           "bytes": mbytes, "tflops": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12}
     del qb, sfb, wsp
     torch.cuda.empty_cache()
+
+
+def run_prefill(m, synth, dev, stream, to_dev, quantize_dev, hbm, fp4_peak, out):
+    import torch
     # prefill: quantize x (4096 x 8192) on the GPU, GEMM against pre-quantised W (28672 x 8192)
     Mp, Np, Kp = 4096, 28672, 8192
     x = to_dev(synth.normal_bf16((Mp, Kp), 2 * 4, 1.0, 1e-3))
@@ -483,7 +523,6 @@ def run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak):
         "gemm_us": ms_g * 1e3, "gemm_tflops": 2.0 * Mp * Np * Kp / (ms_g * 1e-3) / 1e12,
         "gemm_frac": 2.0 * Mp * Np * Kp / (ms_g * 1e-3) / 1e12 / fp4_peak,
         "together_us": ms_t * 1e3}
-    return out
 
 
 if __name__ == "__main__":
