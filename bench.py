@@ -452,10 +452,16 @@ def run_decode(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
         fn = lambda i: m.nvfp4_gemm(xa, sfa, ga, copies[i % 8][0], copies[i % 8][1], gw, M, SQ, SQ, y=y)
         ms = time_graph(fn, 16, 20, stream)
         ms_eager = time_launches(fn, 100, stream)
+        m.nvfp4_tune(m.NVFP4_TUNE_PDL, 1)
+        ms_pdl = time_graph(fn, 16, 20, stream)
+        m.nvfp4_tune(m.NVFP4_TUNE_PDL, 0)
         gbs = wbytes / (ms * 1e-3) / 1e9
+        gbs_pdl = wbytes / (ms_pdl * 1e-3) / 1e9
         out[f"decode_M{M}"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm,
                                "bytes": wbytes, "timing": "CUDA graph of 16 calls over 8 weight copies",
-                               "us_eager_per_launch_events": ms_eager * 1e3}
+                               "us_eager_per_launch_events": ms_eager * 1e3,
+                               "us_pdl": ms_pdl * 1e3, "weight_GBps_pdl": gbs_pdl,
+                               "hbm_frac_pdl": gbs_pdl / hbm}
     del copies, wq, sfw
 
 

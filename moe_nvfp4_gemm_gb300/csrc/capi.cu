@@ -44,7 +44,7 @@ thread_local int g_last_launches = 0;
 
 struct Tune {
   int dense_bn = 0, dense_grid = 0, stream_max_m = 0, stream_split = 0, stream_stages = 0, grouped_grid = 0,
-      grouped_stages = 0, dense_kernel = 0;
+      grouped_stages = 0, dense_kernel = 0, pdl = 0;
 } g_tune;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -192,6 +192,10 @@ int nvfp4_tune(int key, int value) {
       if (value < 0 || value > 2) return NVFP4_ERR_INVALID_ARG;
       g_tune.dense_kernel = value;
       return NVFP4_OK;
+    case NVFP4_TUNE_PDL:
+      if (value < 0 || value > 1) return NVFP4_ERR_INVALID_ARG;
+      g_tune.pdl = value;
+      return NVFP4_OK;
 
     default:
       return NVFP4_ERR_INVALID_ARG;
@@ -311,6 +315,7 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
     }
     if (split > KB) split = KB;
     s.split = split;
+    s.pdl = g_tune.pdl;
     const int stage_bytes = stream_smem_bytes(1, s.x_rows) - 1536;
     int stages = g_tune.stream_stages;
     if (stages == 0) {
@@ -423,6 +428,7 @@ int nvfp4_grouped_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, co
   s.N = static_cast<int>(N);
   s.K = static_cast<int>(K);
   s.split = 1;
+  s.pdl = g_tune.pdl;
   s.x_rows = kGroupTileRows;
   s.acc_cols = kGroupTileRows;
   s.acc_bufs = 2;

@@ -133,6 +133,10 @@ __global__ void __launch_bounds__(192, 1)
   const int NT = (N + 127) / 128;
   const int KB = (K + 255) / 256;
   const int64_t KC4 = K / 64;
+  // With a programmatic dependency the prologue above overlapped the previous kernel.
+  // The grouped path reads the tile list the preparation kernel just wrote, so every
+  // warp waits here; the dense path's producer first requests its first weight tiles.
+  if (GROUPED && p.pdl) griddep_wait();
   int n_items, first, stride;
   if (GROUPED) {
     n_items = __ldg(p.n_tiles) * NT;
@@ -151,6 +155,11 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t ph = 0;
     int issued_phase[16];
     for (int i = 0; i < 16; ++i) issued_phase[i] = -1;
+    // Dense path under a programmatic dependency: the first ring of weight tiles is
+    // requested before waiting for the previous kernel; the token tiles (which that
+    // kernel may have produced) only after it.
+    bool pending = !GROUPED && p.pdl;
+    int pend_stage[16], pend_kb[16], npend = 0;
     Item it;
     for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it) && !*abort_flag; i += stride) {
       const int n16 = (it.rows + 15) >> 4;
@@ -164,19 +173,43 @@ __global__ void __launch_bounds__(192, 1)
           uint8_t* st = smem + s * L.stage_bytes;
           mbar_arrive_expect_tx(&full[s], 16384 + n16 * 2048 + nsub * 1024);
           tma_load_2d(st, &tmW, &full[s], kb * 128, static_cast<int32_t>(wrow0), pol_w);
-          for (int j = 0; j < n16; ++j)
-            tma_load_2d(st + L.x_off + j * 2048, &tmX, &full[s], kb * 128, it.row0 + j * 16, pol_x);
           bulk_load(st + L.sfw_off, sfw + kb * 2048, nsub * 512, &full[s], pol_w);
-          bulk_load(st + L.sfx_off, sfx + kb * 2048, nsub * 512, &full[s], pol_x);
+          if (!pending) {
+            for (int j = 0; j < n16; ++j)
+              tma_load_2d(st + L.x_off + j * 2048, &tmX, &full[s], kb * 128, it.row0 + j * 16, pol_x);
+            bulk_load(st + L.sfx_off, sfx + kb * 2048, nsub * 512, &full[s], pol_x);
+          }
         }
         __syncwarp();
+        if (pending) {
+          pend_stage[npend] = s;
+          pend_kb[npend] = kb;
+          ++npend;
+        }
         issued_phase[s] = ph;
         if (++s == STAGES) {
           s = 0;
           ph ^= 1;
         }
+        if (pending && (npend == STAGES || kb + 1 == it.kb1)) {
+          griddep_wait();
+          if (elect_one()) {
+            for (int j = 0; j < npend; ++j) {
+              const int kbj = pend_kb[j];
+              const int nsub = min(4, (K - kbj * 256) / 64);
+              uint8_t* st = smem + pend_stage[j] * L.stage_bytes;
+              for (int r = 0; r < n16; ++r)
+                tma_load_2d(st + L.x_off + r * 2048, &tmX, &full[pend_stage[j]], kbj * 128, it.row0 + r * 16,
+                            pol_x);
+              bulk_load(st + L.sfx_off, sfx + kbj * 2048, nsub * 512, &full[pend_stage[j]], pol_x);
+            }
+          }
+          __syncwarp();
+          pending = false;
+        }
       }
     }
+    if (p.pdl) griddep_launch_dependents();
     for (int i = 0; i < STAGES; ++i)
       if (issued_phase[i] >= 0) {
         volatile int32_t dummy = 0;
@@ -221,12 +254,14 @@ __global__ void __launch_bounds__(192, 1)
       acc_ph[buf] ^= 1;
       buf = (buf + 1 == p.acc_bufs) ? 0 : buf + 1;
     }
+    if (p.pdl) griddep_launch_dependents();
     if (elect_one()) tc_commit(drain);
     __syncwarp();
     volatile int32_t dummy = 0;
     mbar_wait_warp(drain, 0, &dummy);
   } else {
     constexpr int MAXC = GROUPED ? kGroupTile : 128;
+    if (!GROUPED && p.pdl) griddep_wait();  // the global scales may come from the previous kernel
     const int q = warp & 3;
     const float ga = __ldg(p.ga);
     int buf = 0;
@@ -264,6 +299,7 @@ __global__ void __launch_bounds__(192, 1)
       acc_ph[buf] ^= 1;
       buf = (buf + 1 == p.acc_bufs) ? 0 : buf + 1;
     }
+    if (p.pdl) griddep_launch_dependents();
   }
 
   if (!GROUPED && p.split > 1) {
@@ -378,14 +414,19 @@ static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tm
   cfg.blockDim = dim3(192);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   int nattr = 0;
   if (!GROUPED && a.split > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = a.split;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    nattr = 1;
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = a.split;
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
+  }
+  if (a.pdl) {
+    attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+    ++nattr;
   }
   cfg.attrs = attr;
   cfg.numAttrs = nattr;

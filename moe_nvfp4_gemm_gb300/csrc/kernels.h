@@ -35,6 +35,7 @@ struct StreamArgs {
   int acc_cols;            // TMEM columns per accumulator buffer
   int acc_bufs;
   int tmem_cols;
+  int pdl;                 // launched with programmatic stream serialization
 };
 
 constexpr int kGroupTile = 64;  // tokens of one expert per grouped work item (MMA N <= 64)

@@ -90,6 +90,16 @@ DEVI bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int32_t* abort
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort)) != 0;
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+
+// Blocks until the grids this one depends on have completed and their memory is
+// visible (returns at once when the launch had no programmatic dependency).
+DEVI void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel in the stream start launching (its own griddep_wait still
+// orders its reads after this grid's completion).
+DEVI void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- TMA ----------------------------------------------------------------------
 
 DEVI void prefetch_tmap(const CUtensorMap* m) {

@@ -95,55 +95,74 @@ __global__ void __launch_bounds__(256) k_amax_final(const float* __restrict__ pa
 
 // ---- block quantiser -----------------------------------------------------------
 
-// One CTA = 128 rows x 64 columns (one 512-byte scale tile); one thread = one
-// 16-element block. Thread i: row i/4 of the tile, block i%4. A warp reads 8
-// rows x 128 contiguous bytes; the 512 scale bytes leave as one coalesced tile.
+constexpr int kQuantTiles = 4;  // 512-byte scale tiles (128 rows x 64 columns) per CTA
+
+DEVI void quantize_block(const uint32_t (&w)[8], float g, uint32_t& s, uint2& packed_out) {
+  float f[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    f[2 * j] = bf16lo(w[j]);
+    f[2 * j + 1] = bf16hi(w[j]);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+  const float t = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
+  s = e4m3_encode(t);
+  uint32_t packed[2] = {0u, 0u};
+  if (s != 0) {
+    const float d = __fmul_rn(e4m3_decode(s), g);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t b = e2m1x2_encode(__fdiv_rn(f[2 * j], d), __fdiv_rn(f[2 * j + 1], d));
+      packed[j >> 2] |= b << ((j & 3) * 8);
+    }
+  }
+  packed_out = make_uint2(packed[0], packed[1]);
+}
+
+// One CTA = 128 rows x (64 * kQuantTiles) columns; thread i handles row i/4 and
+// 16-element block i%4 of each 64-column group. All of a thread's loads are issued
+// before any arithmetic (128 bytes in flight per thread); a warp reads 8 rows x 128
+// contiguous bytes per group; each 512-byte scale tile leaves as one coalesced write.
 __global__ void __launch_bounds__(512) k_quantize(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                   const float* __restrict__ gptr,
                                                   uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
-  __shared__ uint32_t tile[128];
+  __shared__ uint32_t tile[kQuantTiles][128];
   const int r_local = threadIdx.x >> 2;
   const int c_local = threadIdx.x & 3;
   const int64_t row = static_cast<int64_t>(blockIdx.y) * 128 + r_local;
-  const int64_t col4 = blockIdx.x;  // which group of four 16-element blocks
-  const int64_t blk = col4 * 4 + c_local;
+  const int64_t kc4 = K / 64;
+  const int64_t col4_0 = static_cast<int64_t>(blockIdx.x) * kQuantTiles;
   const float g = __ldg(gptr);
-  uint32_t s = 0;
-  if (row < M) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + row * K + blk * 16);
-    uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-    uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float f[16];
+  uint4 v[kQuantTiles][2];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      f[2 * j] = bf16lo(w[j]);
-      f[2 * j + 1] = bf16hi(w[j]);
+  for (int t = 0; t < kQuantTiles; ++t) {
+    if (row < M && col4_0 + t < kc4) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + row * K + ((col4_0 + t) * 4 + c_local) * 16);
+      v[t][0] = __ldg(src);
+      v[t][1] = __ldg(src + 1);
     }
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
-    const float t = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
-    s = e4m3_encode(t);
-    uint32_t packed[2] = {0u, 0u};
-    if (s != 0) {
-      const float d = __fmul_rn(e4m3_decode(s), g);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        uint32_t b = e2m1x2_encode(__fdiv_rn(f[2 * j], d), __fdiv_rn(f[2 * j + 1], d));
-        packed[j >> 2] |= b << ((j & 3) * 8);
-      }
-    }
-    uint2* dst = reinterpret_cast<uint2*>(q + row * (K / 2) + blk * 8);
-    *dst = make_uint2(packed[0], packed[1]);
   }
-  // scale byte (r, c) of the tile sits at (r % 32) * 16 + (r / 32) * 4 + c
-  reinterpret_cast<uint8_t*>(tile)[(r_local & 31) * 16 + (r_local >> 5) * 4 + c_local] =
-      static_cast<uint8_t>(s);
+#pragma unroll
+  for (int t = 0; t < kQuantTiles; ++t) {
+    uint32_t s = 0;
+    if (row < M && col4_0 + t < kc4) {
+      const uint32_t w[8] = {v[t][0].x, v[t][0].y, v[t][0].z, v[t][0].w,
+                             v[t][1].x, v[t][1].y, v[t][1].z, v[t][1].w};
+      uint2 packed;
+      quantize_block(w, g, s, packed);
+      *reinterpret_cast<uint2*>(q + row * (K / 2) + ((col4_0 + t) * 4 + c_local) * 8) = packed;
+    }
+    // scale byte (r, c) of a tile sits at (r % 32) * 16 + (r / 32) * 4 + c
+    reinterpret_cast<uint8_t*>(tile[t])[(r_local & 31) * 16 + (r_local >> 5) * 4 + c_local] =
+        static_cast<uint8_t>(s);
+  }
   __syncthreads();
-  if (threadIdx.x < 128) {
-    const int64_t kc4 = K / 64;
-    uint32_t* out = reinterpret_cast<uint32_t*>(sf + (static_cast<int64_t>(blockIdx.y) * kc4 + col4) * 512);
-    out[threadIdx.x] = tile[threadIdx.x];
+  const int t = threadIdx.x >> 7;
+  if (col4_0 + t < kc4) {
+    uint32_t* out = reinterpret_cast<uint32_t*>(sf + (static_cast<int64_t>(blockIdx.y) * kc4 + col4_0 + t) * 512);
+    out[threadIdx.x & 127] = tile[t][threadIdx.x & 127];
   }
 }
 
@@ -171,7 +190,7 @@ cudaError_t launch_amax(const uint16_t* x, int64_t n, float* amax_out, float* g_
 
 cudaError_t launch_quantize(const uint16_t* x, int64_t M, int64_t K, const float* g, uint8_t* q,
                             uint8_t* sf, cudaStream_t st) {
-  dim3 grid(static_cast<unsigned>(K / 64), static_cast<unsigned>((M + 127) / 128));
+  dim3 grid(static_cast<unsigned>((K / 64 + kQuantTiles - 1) / kQuantTiles), static_cast<unsigned>((M + 127) / 128));
   k_quantize<<<grid, 512, 0, st>>>(x, M, K, g, q, sf);
   return cudaGetLastError();
 }

@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(autouse=True)
 def _reset_tuning():
     yield
-    for key in range(1, 9):
+    for key in range(1, 10):
         m.nvfp4_tune(key, 0)
 
 
@@ -121,3 +121,31 @@ def test_empty_m_is_noop():
     A, B = dense_case(1, 128, 256, 4)
     y = torch.full((0, 128), 7.0, dtype=torch.bfloat16, device=dev())
     m.nvfp4_gemm(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, 0, 128, 256, y=y)
+
+
+def test_programmatic_dependent_launch_keeps_stream_order():
+    # Eight back-to-back decode calls (PDL on) in one CUDA graph, alternating between two
+    # problems, all writing the same y: the last call's result must win, and each
+    # call's output must be the problem's own result (the weights are prefetched before
+    # the dependency wait, the tokens, scales and the output write come after it).
+    A1, B1 = dense_case(16, 512, 1024, 31, 1.0, 1e-3, 0.02)
+    A2, B2 = dense_case(16, 512, 1024, 32, 1.0, 1e-3, 0.02)
+    ref1 = _run(A1, B1).clone()
+    ref2 = _run(A2, B2).clone()
+    m.nvfp4_tune(m.NVFP4_TUNE_PDL, 1)
+    y = torch.empty_like(ref1)
+    outs = [torch.empty_like(ref1) for _ in range(8)]
+    calls = [(A1, B1), (A2, B2)] * 4
+    for A, B in calls[:2]:  # warm up outside capture
+        m.nvfp4_gemm(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, 16, 512, 1024, y=y)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i, (A, B) in enumerate(calls):
+            m.nvfp4_gemm(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, 16, 512, 1024, y=y)
+            outs[i].copy_(y)
+    g.replay()
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        assert torch.equal(o, ref1 if i % 2 == 0 else ref2), i
+    assert torch.equal(y, ref2)
