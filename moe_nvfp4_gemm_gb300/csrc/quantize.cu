@@ -112,9 +112,28 @@ DEVI void quantize_block(const uint32_t (&w)[8], float g, uint32_t& s, uint2& pa
   uint32_t packed[2] = {0u, 0u};
   if (s != 0) {
     const float d = __fmul_rn(e4m3_decode(s), g);
+    // x / d correctly rounded without a division per element: y = RN(1/d), q0 = RN(x y)
+    // is within one ulp of x / d, the remainder x - q0 d is exact (fma), and
+    // RN(q0 + rem * y) = RN(x / d) by Markstein's theorem when nothing over- or
+    // underflows. Blocks outside that range take IEEE division; exact zeros keep
+    // their sign.
+    const float y = __frcp_rn(d);
+    const bool fast = d > 1e-30f && d < 1e30f && __fmul_rn(amax, y) < 1e30f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      uint32_t b = e2m1x2_encode(__fdiv_rn(f[2 * j], d), __fdiv_rn(f[2 * j + 1], d));
+      float v[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float x = f[2 * j + h];
+        if (fast) {
+          const float q0 = __fmul_rn(x, y);
+          const float r = __fmaf_rn(-q0, d, x);
+          v[h] = (x == 0.0f) ? x : __fmaf_rn(r, y, q0);
+        } else {
+          v[h] = __fdiv_rn(x, d);
+        }
+      }
+      uint32_t b = e2m1x2_encode(v[0], v[1]);
       packed[j >> 2] |= b << ((j & 3) * 8);
     }
   }

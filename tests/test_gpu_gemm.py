@@ -124,28 +124,31 @@ def test_empty_m_is_noop():
 
 
 def test_programmatic_dependent_launch_keeps_stream_order():
-    # Eight back-to-back decode calls (PDL on) in one CUDA graph, alternating between two
-    # problems, all writing the same y: the last call's result must win, and each
-    # call's output must be the problem's own result (the weights are prefetched before
-    # the dependency wait, the tokens, scales and the output write come after it).
+    # Back-to-back decode calls with programmatic dependent launch inside one CUDA graph,
+    # alternating between two problems: (1) each writing its own output must produce the
+    # problem's own result; (2) all writing the same output, the last call's result must
+    # win (every output write is ordered after the previous call's completion).
     A1, B1 = dense_case(16, 512, 1024, 31, 1.0, 1e-3, 0.02)
     A2, B2 = dense_case(16, 512, 1024, 32, 1.0, 1e-3, 0.02)
     ref1 = _run(A1, B1).clone()
     ref2 = _run(A2, B2).clone()
     m.nvfp4_tune(m.NVFP4_TUNE_PDL, 1)
+    calls = [(A1, B1), (A2, B2)] * 4 + [(A1, B1)]
+    outs = [torch.empty_like(ref1) for _ in calls]
     y = torch.empty_like(ref1)
-    outs = [torch.empty_like(ref1) for _ in range(8)]
-    calls = [(A1, B1), (A2, B2)] * 4
+    gemm = lambda A, B, out: m.nvfp4_gemm(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, 16, 512, 1024, y=out)
     for A, B in calls[:2]:  # warm up outside capture
-        m.nvfp4_gemm(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, 16, 512, 1024, y=y)
+        gemm(A, B, y)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        for i, (A, B) in enumerate(calls):
-            m.nvfp4_gemm(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, 16, 512, 1024, y=y)
-            outs[i].copy_(y)
+        for (A, B), o in zip(calls, outs):
+            gemm(A, B, o)
+        for A, B in calls:
+            gemm(A, B, y)
+    y.fill_(0)
     g.replay()
     torch.cuda.synchronize()
     for i, o in enumerate(outs):
         assert torch.equal(o, ref1 if i % 2 == 0 else ref2), i
-    assert torch.equal(y, ref2)
+    assert torch.equal(y, ref1)

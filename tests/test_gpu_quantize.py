@@ -103,3 +103,30 @@ def test_amax_zero_tensor_gives_unit_scale():
     x = torch.zeros(1000, dtype=torch.bfloat16, device=dev())
     amax, g = m.nvfp4_amax(x)
     assert amax.item() == 0.0 and g.item() == 1.0
+
+
+def test_quantize_quotients_near_every_rounding_boundary():
+    # Per block: a random global scale g and block maximum, then elements whose quotients
+    # x / (E4M3(s) g) fall within a few ulps of every E2M1 rounding threshold (0.25, 0.75,
+    # 1.25, 1.75, 2.5, 3.5, 5) and the saturation point 6, with both signs. The quantiser
+    # must round each of them exactly as the oracle's float32 division does.
+    rng = np.random.default_rng(77)
+    rows = 256
+    K = 1024
+    x = np.zeros((rows, K), dtype=np.float32)
+    g = np.float32(rng.uniform(1e-3, 2.0))
+    thresholds = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0], dtype=np.float32)
+    for r in range(rows):
+        for b in range(K // 16):
+            amax = np.float32(rng.uniform(0.5, 3000.0) * g)
+            t = np.float32(np.float32(amax / np.float32(6.0)) / g)
+            s = oracle.e4m3_encode(min(float(t), 448.0))
+            d = np.float32(np.float32(oracle.e4m3_value(s)) * g)
+            thr = rng.choice(thresholds, size=15)
+            jitter = rng.integers(-3, 4, size=15).astype(np.float64)
+            vals = thr.astype(np.float64) * float(d) * (1.0 + jitter * 2.0 ** -9)
+            vals *= rng.choice([-1.0, 1.0], size=15)
+            blk = np.concatenate([[amax], vals]).astype(np.float32)
+            x[r, b * 16:(b + 1) * 16] = blk
+    xb = synth.f32_to_bf16_bits(x)
+    _quantize_and_compare(xb, g)
