@@ -316,7 +316,7 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
     if (split > KB) split = KB;
     s.split = split;
     s.pdl = g_tune.pdl;
-    const int stage_bytes = stream_smem_bytes(1, s.x_rows) - 1536;
+    const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0) - 1536;
     int stages = g_tune.stream_stages;
     if (stages == 0) {
       stages = (110 * 1024 - 1536) / stage_bytes;  // two CTAs per SM
@@ -324,9 +324,9 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
       if (stages > tmem_room) stages = tmem_room;
       if (stages < 2) stages = 2;
     }
-    // split-K partials reuse the stage ring: it must hold x_rows x 128 fp32
-    while (split > 1 && stages * stage_bytes < s.x_rows * 512) ++stages;
-    if (stream_smem_bytes(stages, s.x_rows) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    // the split-K partials (M x 128 fp32) reuse the stage ring
+    while (split > 1 && stages * stage_bytes < s.M * 512) ++stages;
+    if (stream_smem_bytes(stages, s.x_rows, 0) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     s.stages = stages;
     s.tmem_cols = pow2_at_least(s.acc_cols + 32 * stages);
     if (s.tmem_cols > 512) return NVFP4_ERR_UNSUPPORTED_SHAPE;
@@ -432,13 +432,13 @@ int nvfp4_grouped_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, co
   s.x_rows = kGroupTileRows;
   s.acc_cols = kGroupTileRows;
   s.acc_bufs = 2;
-  const int stage_bytes = stream_smem_bytes(1, s.x_rows) - 1536;
+  const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0) - 1536;
   int stages = g_tune.grouped_stages;
   if (stages == 0) stages = (kSmemLimit - 1536) / stage_bytes;
   const int tmem_room = (512 - 2 * s.acc_cols) / 32;
   if (stages > tmem_room) stages = tmem_room;
   if (stages > 16) stages = 16;
-  if (stream_smem_bytes(stages, s.x_rows) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (stream_smem_bytes(stages, s.x_rows, 0) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   s.stages = stages;
   s.tmem_cols = pow2_at_least(2 * s.acc_cols + 32 * stages);
   const int grid = g_tune.grouped_grid ? g_tune.grouped_grid : d.sms;

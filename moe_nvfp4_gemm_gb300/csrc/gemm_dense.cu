@@ -30,6 +30,13 @@
 namespace nvfp4 {
 
 constexpr int kDenseThreads = 320;  // producer, MMA, 8 epilogue warps
+// CTA-pair kernel: + one warp that waits for each stage's TMA bytes and hands the
+// stage to the MMA warp through a named barrier. An mbarrier wait in the MMA-issuing
+// warp stalls the tensor pipe (hundreds of cycles per wait, measured on GB300); the
+// named-barrier handoff does not.
+constexpr int kPairThreads = 352;
+constexpr int kWaiterWarp = 10;
+constexpr uint32_t kStageHandoffBarrier = 1;
 
 template <int BN, int STAGES>
 struct DenseCfg {
@@ -221,7 +228,7 @@ struct PairCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-__global__ void __launch_bounds__(kDenseThreads, 1)
+__global__ void __launch_bounds__(kPairThreads, 1)
     k_gemm_dense_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                       const DenseArgs p) {
@@ -308,43 +315,63 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
           volatile int32_t dummy = 0;
           mbar_wait_warp(&full[i], issued_phase[i], &dummy);
         }
-  } else if (warp == 1) {
+  } else if (warp == kWaiterWarp) {
+    // Stage handoff: wait for the stage's bytes, then meet the MMA warp. Both warps
+    // run exactly tiles x KB iterations (also after an abort) so that the named
+    // barrier, which cannot time out, always pairs.
     if (leader) {
-      const uint32_t idesc = idesc_nvf4(256, 256);
       int s = 0;
-      uint32_t ph = 0, acc_ph = 0;
-      for (int t = pair; t < tiles && !*abort_flag; t += npairs) {
-        if (!mbar_wait_warp(tempty, acc_ph ^ 1, abort_flag)) break;
-        tc_fence_after();
+      uint32_t ph = 0;
+      for (int t = pair; t < tiles; t += npairs) {
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_warp(&full[s], ph, abort_flag)) break;
-          tc_fence_after();
-          if (elect_one()) {
-            const int nsub = min(4, (K - kb * 256) / 64);
-            const uint32_t a_addr = smem_u32(smem + s * C::STAGE_BYTES);
-            const uint32_t b_addr = a_addr + C::A_BYTES;
-            const uint32_t sfa_addr = b_addr + C::B_BYTES;
-            const uint32_t sfb_addr = sfa_addr + C::SFA_BYTES;
-            const uint32_t sf_col = tmem + 256 + s * C::SF_COLS;
-            for (int kk = 0; kk < nsub; ++kk) {
-              tc_cp_32x128b_x4_pair(sf_col + kk * 4, desc_sf(sfa_addr + kk * 512));
-              tc_cp_32x128b_x4_pair(sf_col + 16 + kk * 8, desc_sf(sfb_addr + kk * 512));
-              tc_cp_32x128b_x4_pair(sf_col + 16 + kk * 8 + 4, desc_sf(sfb_addr + 2048 + kk * 512));
-            }
-            const uint64_t adesc = desc_sw128(a_addr), bdesc = desc_sw128(b_addr);
-            for (int kk = 0; kk < nsub; ++kk)
-              tc_mma_nvf4_pair(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, sf_col + kk * 4, sf_col + 16 + kk * 8,
-                               (kb | kk) != 0);
-            tc_commit_pair(&empty[s], 3);
-          }
-          __syncwarp();
+          if (__all_sync(0xffffffffu, *abort_flag == 0)) mbar_wait_warp(&full[s], ph, abort_flag);
+          named_sync(kStageHandoffBarrier, 64);
           if (++s == STAGES) {
             s = 0;
             ph ^= 1;
           }
         }
-        if (elect_one()) tc_commit_pair(tfull, 3);
-        __syncwarp();
+      }
+    }
+  } else if (warp == 1) {
+    if (leader) {
+      const uint32_t idesc = idesc_nvf4(256, 256);
+      int s = 0;
+      uint32_t acc_ph = 0;
+      for (int t = pair; t < tiles; t += npairs) {
+        const bool tile_ok =
+            __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(tempty, acc_ph ^ 1, abort_flag);
+        tc_fence_after();
+        for (int kb = 0; kb < KB; ++kb) {
+          named_sync(kStageHandoffBarrier, 64);  // the waiter saw this stage's bytes land
+          tc_fence_after();
+          if (tile_ok && __all_sync(0xffffffffu, *abort_flag == 0)) {
+            if (elect_one()) {
+              const int nsub = min(4, (K - kb * 256) / 64);
+              const uint32_t a_addr = smem_u32(smem + s * C::STAGE_BYTES);
+              const uint32_t b_addr = a_addr + C::A_BYTES;
+              const uint32_t sfa_addr = b_addr + C::B_BYTES;
+              const uint32_t sfb_addr = sfa_addr + C::SFA_BYTES;
+              const uint32_t sf_col = tmem + 256 + s * C::SF_COLS;
+              for (int kk = 0; kk < nsub; ++kk) {
+                tc_cp_32x128b_x4_pair(sf_col + kk * 4, desc_sf(sfa_addr + kk * 512));
+                tc_cp_32x128b_x4_pair(sf_col + 16 + kk * 8, desc_sf(sfb_addr + kk * 512));
+                tc_cp_32x128b_x4_pair(sf_col + 16 + kk * 8 + 4, desc_sf(sfb_addr + 2048 + kk * 512));
+              }
+              const uint64_t adesc = desc_sw128(a_addr), bdesc = desc_sw128(b_addr);
+              for (int kk = 0; kk < nsub; ++kk)
+                tc_mma_nvf4_pair(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, sf_col + kk * 4, sf_col + 16 + kk * 8,
+                                 (kb | kk) != 0);
+              tc_commit_pair(&empty[s], 3);
+            }
+            __syncwarp();
+          }
+          if (++s == STAGES) s = 0;
+        }
+        if (tile_ok) {
+          if (elect_one()) tc_commit_pair(tfull, 3);
+          __syncwarp();
+        }
         acc_ph ^= 1;
       }
       if (elect_one()) tc_commit_pair(drain, 1);
@@ -407,7 +434,7 @@ cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, co
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kDenseThreads);
+  cfg.blockDim = dim3(kPairThreads);
   cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];

@@ -88,14 +88,24 @@ DEVI bool get_item(const StreamArgs& p, int i, int n_items, int NT, int KB, Item
   return true;
 }
 
+// Warp roles: 0 TMA producer, 1 MMA issuer, 2-5 epilogue, 6 stage waiter (waits for a
+// stage's bytes and hands it to the MMA warp through a named barrier, so that the
+// MMA-issuing warp itself never waits on an mbarrier per stage).
+constexpr int kStreamThreads = 224;
+constexpr int kStreamWaiterWarp = 6;
+constexpr uint32_t kStreamHandoffBarrier = 1;
+
 template <bool GROUPED>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kStreamThreads, 2)
     k_gemm_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                   const StreamArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const StreamLayout L(p.x_rows);
   const int STAGES = p.stages;
+  // split-K partial sums of this CTA [token][128 rows] fp32: the stage ring is reused
+  // (one item per CTA; every stage has been consumed when the epilogue runs)
+  float* part = reinterpret_cast<float*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * L.stage_bytes);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;  // [2]
@@ -215,42 +225,60 @@ __global__ void __launch_bounds__(192, 1)
         volatile int32_t dummy = 0;
         mbar_wait_warp(&full[i], issued_phase[i], &dummy);
       }
-  } else if (warp == 1) {
-    int s = 0, buf = 0;
-    uint32_t ph = 0, acc_ph[2] = {0, 0};
+  } else if (warp == kStreamWaiterWarp) {
+    // Same item and stage sequence as the MMA warp, also after an abort, so that the
+    // named barrier (no time-out) always pairs.
+    int s = 0;
+    uint32_t ph = 0;
     Item it;
-    for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it) && !*abort_flag; i += stride) {
-      const int n_mma = ((it.rows + 15) >> 4) * 16;
-      const uint32_t idesc = idesc_nvf4(128, n_mma);
-      const uint32_t acc = tmem + buf * p.acc_cols;
-      if (!mbar_wait_warp(&tempty[buf], acc_ph[buf] ^ 1, abort_flag)) break;
-      tc_fence_after();
+    for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it); i += stride) {
       for (int kb = it.kb0; kb < it.kb1; ++kb) {
-        if (!mbar_wait_warp(&full[s], ph, abort_flag)) break;
-        tc_fence_after();
-        if (elect_one()) {
-          const int nsub = min(4, (K - kb * 256) / 64);
-          const uint32_t w_addr = smem_u32(smem + s * L.stage_bytes);
-          const uint32_t x_addr = w_addr + L.x_off;
-          const uint32_t sf_col = sf_base + s * 32;
-          for (int kk = 0; kk < nsub; ++kk) {
-            tc_cp_32x128b_x4(sf_col + kk * 4, desc_sf(w_addr + L.sfw_off + kk * 512));
-            tc_cp_32x128b_x4(sf_col + 16 + kk * 4, desc_sf(w_addr + L.sfx_off + kk * 512));
-          }
-          const uint64_t wdesc = desc_sw128(w_addr), xdesc = desc_sw128(x_addr);
-          for (int kk = 0; kk < nsub; ++kk)
-            tc_mma_nvf4(acc, wdesc + 2 * kk, xdesc + 2 * kk, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4,
-                        (kb != it.kb0) || (kk != 0));
-          tc_commit(&empty[s]);
-        }
-        __syncwarp();
+        if (__all_sync(0xffffffffu, *abort_flag == 0)) mbar_wait_warp(&full[s], ph, abort_flag);
+        named_sync(kStreamHandoffBarrier, 64);
         if (++s == STAGES) {
           s = 0;
           ph ^= 1;
         }
       }
-      if (elect_one()) tc_commit(&tfull[buf]);
-      __syncwarp();
+    }
+  } else if (warp == 1) {
+    int s = 0, buf = 0;
+    uint32_t acc_ph[2] = {0, 0};
+    Item it;
+    for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it); i += stride) {
+      const int n_mma = ((it.rows + 15) >> 4) * 16;
+      const uint32_t idesc = idesc_nvf4(128, n_mma);
+      const uint32_t acc = tmem + buf * p.acc_cols;
+      const bool item_ok =
+          __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(&tempty[buf], acc_ph[buf] ^ 1, abort_flag);
+      tc_fence_after();
+      for (int kb = it.kb0; kb < it.kb1; ++kb) {
+        named_sync(kStreamHandoffBarrier, 64);  // the waiter saw this stage's bytes land
+        tc_fence_after();
+        if (item_ok && __all_sync(0xffffffffu, *abort_flag == 0)) {
+          if (elect_one()) {
+            const int nsub = min(4, (K - kb * 256) / 64);
+            const uint32_t w_addr = smem_u32(smem + s * L.stage_bytes);
+            const uint32_t x_addr = w_addr + L.x_off;
+            const uint32_t sf_col = sf_base + s * 32;
+            for (int kk = 0; kk < nsub; ++kk) {
+              tc_cp_32x128b_x4(sf_col + kk * 4, desc_sf(w_addr + L.sfw_off + kk * 512));
+              tc_cp_32x128b_x4(sf_col + 16 + kk * 4, desc_sf(w_addr + L.sfx_off + kk * 512));
+            }
+            const uint64_t wdesc = desc_sw128(w_addr), xdesc = desc_sw128(x_addr);
+            for (int kk = 0; kk < nsub; ++kk)
+              tc_mma_nvf4(acc, wdesc + 2 * kk, xdesc + 2 * kk, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4,
+                          (kb != it.kb0) || (kk != 0));
+            tc_commit(&empty[s]);
+          }
+          __syncwarp();
+        }
+        if (++s == STAGES) s = 0;
+      }
+      if (item_ok) {
+        if (elect_one()) tc_commit(&tfull[buf]);
+        __syncwarp();
+      }
       acc_ph[buf] ^= 1;
       buf = (buf + 1 == p.acc_bufs) ? 0 : buf + 1;
     }
@@ -260,13 +288,12 @@ __global__ void __launch_bounds__(192, 1)
     volatile int32_t dummy = 0;
     mbar_wait_warp(drain, 0, &dummy);
   } else {
-    constexpr int MAXC = GROUPED ? kGroupTile : 128;
+    constexpr int MAXC = kGroupTile;
     if (!GROUPED && p.pdl) griddep_wait();  // the global scales may come from the previous kernel
     const int q = warp & 3;
     const float ga = __ldg(p.ga);
     int buf = 0;
     uint32_t acc_ph[2] = {0, 0};
-    float* red = reinterpret_cast<float*>(smem);  // split-K partials (stage memory, reused)
     Item it;
     for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it); i += stride) {
       if (!mbar_wait_warp(&tfull[buf], acc_ph[buf], abort_flag)) break;
@@ -275,26 +302,48 @@ __global__ void __launch_bounds__(192, 1)
       const int wrow = it.wt * 128 + q * 32 + lane;  // output column
       const int n_mma = ((it.rows + 15) >> 4) * 16;
       const bool has_k = it.kb1 > it.kb0;
-      // all of this item's columns into registers, then release the accumulator
-      uint32_t r[MAXC];
+      const uint32_t tbase = tmem + buf * p.acc_cols + (static_cast<uint32_t>(q * 32) << 16);
+      if (GROUPED) {
+        // all of this item's columns into registers, release the accumulator for the
+        // next item's MMAs, then store
+        uint32_t r[MAXC];
 #pragma unroll
-      for (int c = 0; c < MAXC; c += 32)
-        if (c < n_mma) tmem_ld32(tmem + buf * p.acc_cols + (static_cast<uint32_t>(q * 32) << 16) + c, r + c);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (elect_one()) mbar_arrive(&tempty[buf]);
-      __syncwarp();
-      if (!GROUPED && p.split > 1) {
+        for (int c = 0; c < MAXC; c += 32)
+          if (c < n_mma) tmem_ld32(tbase + c, r + c);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (elect_one()) mbar_arrive(&tempty[buf]);
+        __syncwarp();
+        if (wrow < N) {
 #pragma unroll
-        for (int j = 0; j < MAXC; ++j)
-          if (j < n_mma) red[j * 128 + q * 32 + lane] = has_k ? __uint_as_float(r[j]) : 0.0f;
-      } else if (wrow < N) {
+          for (int j = 0; j < MAXC; ++j)
+            if (j < it.rows)
+              p.y[static_cast<int64_t>(it.row0 + j) * N + wrow] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j]) * alpha));
+        }
+      } else {
+        // one item per CTA: drain 32 columns at a time (fewer live registers)
+        for (int c = 0; c < n_mma; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(tbase + c, r);
+          tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < MAXC; ++j)
-          if (j < it.rows)
-            p.y[static_cast<int64_t>(it.row0 + j) * N + wrow] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j]) * alpha));
+          for (int j = 0; j < 32; ++j) {
+            const int tok = c + j;
+            if (tok < it.rows) {
+              if (p.split > 1)
+                part[tok * 128 + q * 32 + lane] = has_k ? __uint_as_float(r[j]) : 0.0f;
+              else if (wrow < N)
+                p.y[static_cast<int64_t>(it.row0 + tok) * N + wrow] =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j]) * alpha));
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (elect_one()) mbar_arrive(&tempty[buf]);
+        __syncwarp();
       }
       acc_ph[buf] ^= 1;
       buf = (buf + 1 == p.acc_bufs) ? 0 : buf + 1;
@@ -303,16 +352,18 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   if (!GROUPED && p.split > 1) {
-    // Sum the S partial tiles of this cluster through distributed shared memory;
-    // CTA rank r finishes tokens r, r + S, ...
+    // Sum the S partial tiles of this cluster through distributed shared memory, in
+    // rank order; CTA rank r finishes tokens r, r + S, ... A second barrier keeps every
+    // CTA's partials alive until they have been read. (Issuing all remote loads before
+    // summing measured ~3 us slower per call than this loop.)
     cluster_sync_all();
-    if (warp >= 2) {
+    if (warp >= 2 && warp < kStreamWaiterWarp) {
       const int q = warp & 3;
       const uint32_t rank = cluster_rank();
       const int wt = blockIdx.x / p.split;
       const int wrow = wt * 128 + q * 32 + lane;
       const float alpha = __ldg(p.ga) * __ldg(p.gb);
-      const uint32_t red_addr = smem_u32(smem);
+      const uint32_t red_addr = smem_u32(part);
       for (int tok = rank; tok < p.M; tok += p.split) {
         float v = 0.0f;
         for (int c = 0; c < p.split; ++c) v += ld_dsmem_f32(red_addr + (tok * 128 + q * 32 + lane) * 4, c);
@@ -411,7 +462,7 @@ static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tm
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(kStreamThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -435,7 +486,9 @@ static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tm
   return cudaGetLastError();
 }
 
-int stream_smem_bytes(int stages, int x_rows) { return stages * StreamLayout(x_rows).stage_bytes + 1024 + 512; }
+int stream_smem_bytes(int stages, int x_rows, int recv_bytes) {
+  return stages * StreamLayout(x_rows).stage_bytes + recv_bytes + 1024 + 512;
+}
 
 cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, bool grouped, int grid,
                           cudaStream_t st) {

@@ -38,6 +38,7 @@ struct StreamArgs {
   int pdl;                 // launched with programmatic stream serialization
 };
 
+
 constexpr int kGroupTile = 64;  // tokens of one expert per grouped work item (MMA N <= 64)
 
 cudaError_t launch_amax(const uint16_t* x, int64_t n, float* amax_out, float* g_out, float* partial,
@@ -54,7 +55,7 @@ cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const 
 cudaError_t launch_grouped_prep(const int32_t* offsets, int E, int M_total, int K, const uint8_t* sfx,
                                 int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
                                 cudaStream_t st);
-int stream_smem_bytes(int stages, int x_rows);
+int stream_smem_bytes(int stages, int x_rows, int recv_bytes);
 
 // Raises `func`'s dynamic shared-memory limit to the opt-in maximum, once per
 // (kernel, device); later calls only look the pair up.

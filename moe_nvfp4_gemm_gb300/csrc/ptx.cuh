@@ -90,6 +90,12 @@ DEVI bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int32_t* abort
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort)) != 0;
 }
 
+// Named CTA barrier `id` over `nthreads` threads (whole warps). Used in lockstep by
+// two warps that run exactly the same number of iterations: it has no time-out.
+DEVI void named_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ---- programmatic dependent launch ---------------------------------------------
 
 // Blocks until the grids this one depends on have completed and their memory is
