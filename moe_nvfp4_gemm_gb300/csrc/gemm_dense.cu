@@ -156,16 +156,20 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
           const uint32_t sfa_addr = b_addr + C::B_BYTES;
           const uint32_t sfb_addr = sfa_addr + C::SFA_BYTES;
           const uint32_t sf_col = tmem + BN + s * C::SF_COLS;
-          for (int kk = 0; kk < nsub; ++kk) {
-            tc_cp_32x128b_x4(sf_col + kk * 4, desc_sf(sfa_addr + kk * 512));
 #pragma unroll
-            for (int g = 0; g < C::GROUPS; ++g)
-              tc_cp_32x128b_x4(sf_col + 16 + kk * 4 * C::GROUPS + g * 4, desc_sf(sfb_addr + g * 2048 + kk * 512));
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            if (kk < nsub) {
+              tc_cp_32x128b_x4(sf_col + kk * 4, desc_sf(sfa_addr + kk * 512));
+#pragma unroll
+              for (int g = 0; g < C::GROUPS; ++g)
+                tc_cp_32x128b_x4(sf_col + 16 + kk * 4 * C::GROUPS + g * 4, desc_sf(sfb_addr + g * 2048 + kk * 512));
+            }
           const uint64_t adesc = desc_sw128(a_addr), bdesc = desc_sw128(b_addr);
-          for (int kk = 0; kk < nsub; ++kk)
-            tc_mma_nvf4(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, sf_col + kk * 4,
-                        sf_col + 16 + kk * 4 * C::GROUPS, (kb | kk) != 0);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            if (kk < nsub)
+              tc_mma_nvf4(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, sf_col + kk * 4,
+                          sf_col + 16 + kk * 4 * C::GROUPS, (kb | kk) != 0);
           tc_commit(&empty[s]);
         }
         __syncwarp();
@@ -187,6 +191,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     const int q = warp & 3;         // TMEM lane quarter this warp may read
     const int h = (warp - 2) >> 2;  // which half of the tile's columns
     const float alpha = __ldg(p.ga) * __ldg(p.gb);
+    const bool wide = N % 16 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 31) == 0;
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
       const int m_blk = t % mt, n_blk = t / mt;
@@ -194,7 +199,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       tc_fence_after();
       const int row = m_blk * 128 + q * 32 + lane;
       drain_accumulator<BN / 2>(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * (BN / 2), alpha,
-                                p.y + static_cast<int64_t>(row) * N, row < M, n_blk * BN + h * (BN / 2), N,
+                                p.y + static_cast<int64_t>(row) * N, row < M, n_blk * BN + h * (BN / 2), N, wide,
                                 [&] {
                                   if (elect_one()) mbar_arrive(tempty);
                                   __syncwarp();
@@ -316,16 +321,23 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           mbar_wait_warp(&full[i], issued_phase[i], &dummy);
         }
   } else if (warp == kWaiterWarp) {
-    // Stage handoff: wait for the stage's bytes, then meet the MMA warp. Both warps
-    // run exactly tiles x KB iterations (also after an abort) so that the named
-    // barrier, which cannot time out, always pairs.
+    // Owns every wait in front of the MMA warp: the accumulator being free at the
+    // start of each tile, then each stage's bytes landing. The verdict (false after
+    // an abort or a time-out) reaches the MMA warp through bar.red, so the MMA
+    // warp touches neither an mbarrier nor shared memory between its issues. Both
+    // warps run exactly tiles x KB iterations (also after an abort) so that the
+    // named barrier, which cannot time out, always pairs.
     if (leader) {
       int s = 0;
-      uint32_t ph = 0;
+      uint32_t ph = 0, acc_ph = 0;
       for (int t = pair; t < tiles; t += npairs) {
+        const bool tile_ok =
+            __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(tempty, acc_ph ^ 1, abort_flag);
+        acc_ph ^= 1;
         for (int kb = 0; kb < KB; ++kb) {
-          if (__all_sync(0xffffffffu, *abort_flag == 0)) mbar_wait_warp(&full[s], ph, abort_flag);
-          named_sync(kStageHandoffBarrier, 64);
+          const bool ok =
+              tile_ok && __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(&full[s], ph, abort_flag);
+          named_sync_and(kStageHandoffBarrier, 64, ok);
           if (++s == STAGES) {
             s = 0;
             ph ^= 1;
@@ -337,31 +349,35 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     if (leader) {
       const uint32_t idesc = idesc_nvf4(256, 256);
       int s = 0;
-      uint32_t acc_ph = 0;
       for (int t = pair; t < tiles; t += npairs) {
-        const bool tile_ok =
-            __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(tempty, acc_ph ^ 1, abort_flag);
-        tc_fence_after();
+        bool tile_ok = true;
         for (int kb = 0; kb < KB; ++kb) {
-          named_sync(kStageHandoffBarrier, 64);  // the waiter saw this stage's bytes land
+          const bool ok = named_sync_and(kStageHandoffBarrier, 64, true);
+          tile_ok = tile_ok && ok;
           tc_fence_after();
-          if (tile_ok && __all_sync(0xffffffffu, *abort_flag == 0)) {
+          if (ok) {
             if (elect_one()) {
+              // Fully unrolled: a data-dependent trip count here makes the elected
+              // lane issue each tcgen05 instruction on its own, far more slowly.
               const int nsub = min(4, (K - kb * 256) / 64);
               const uint32_t a_addr = smem_u32(smem + s * C::STAGE_BYTES);
               const uint32_t b_addr = a_addr + C::A_BYTES;
               const uint32_t sfa_addr = b_addr + C::B_BYTES;
               const uint32_t sfb_addr = sfa_addr + C::SFA_BYTES;
               const uint32_t sf_col = tmem + 256 + s * C::SF_COLS;
-              for (int kk = 0; kk < nsub; ++kk) {
-                tc_cp_32x128b_x4_pair(sf_col + kk * 4, desc_sf(sfa_addr + kk * 512));
-                tc_cp_32x128b_x4_pair(sf_col + 16 + kk * 8, desc_sf(sfb_addr + kk * 512));
-                tc_cp_32x128b_x4_pair(sf_col + 16 + kk * 8 + 4, desc_sf(sfb_addr + 2048 + kk * 512));
-              }
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                if (kk < nsub) {
+                  tc_cp_32x128b_x4_pair(sf_col + kk * 4, desc_sf(sfa_addr + kk * 512));
+                  tc_cp_32x128b_x4_pair(sf_col + 16 + kk * 8, desc_sf(sfb_addr + kk * 512));
+                  tc_cp_32x128b_x4_pair(sf_col + 16 + kk * 8 + 4, desc_sf(sfb_addr + 2048 + kk * 512));
+                }
               const uint64_t adesc = desc_sw128(a_addr), bdesc = desc_sw128(b_addr);
-              for (int kk = 0; kk < nsub; ++kk)
-                tc_mma_nvf4_pair(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, sf_col + kk * 4, sf_col + 16 + kk * 8,
-                                 (kb | kk) != 0);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                if (kk < nsub)
+                  tc_mma_nvf4_pair(tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, sf_col + kk * 4, sf_col + 16 + kk * 8,
+                                   (kb | kk) != 0);
               tc_commit_pair(&empty[s], 3);
             }
             __syncwarp();
@@ -372,7 +388,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           if (elect_one()) tc_commit_pair(tfull, 3);
           __syncwarp();
         }
-        acc_ph ^= 1;
       }
       if (elect_one()) tc_commit_pair(drain, 1);
       __syncwarp();
@@ -382,6 +397,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   } else {
     const int q = warp & 3, h = (warp - 2) >> 2;
     const float alpha = __ldg(p.ga) * __ldg(p.gb);
+    const bool wide = N % 16 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 31) == 0;
     const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
     uint32_t acc_ph = 0;
     for (int t = pair; t < tiles; t += npairs) {
@@ -390,7 +406,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       tc_fence_after();
       const int row = m_blk * 256 + rank * 128 + q * 32 + lane;
       drain_accumulator<128>(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128, alpha,
-                             p.y + static_cast<int64_t>(row) * N, row < M, n_blk * 256 + h * 128, N, [&] {
+                             p.y + static_cast<int64_t>(row) * N, row < M, n_blk * 256 + h * 128, N, wide, [&] {
                                if (elect_one()) mbar_arrive_cluster(tempty_leader);
                                __syncwarp();
                              });

@@ -226,15 +226,24 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         mbar_wait_warp(&full[i], issued_phase[i], &dummy);
       }
   } else if (warp == kStreamWaiterWarp) {
-    // Same item and stage sequence as the MMA warp, also after an abort, so that the
-    // named barrier (no time-out) always pairs.
-    int s = 0;
+    // Owns every wait in front of the MMA warp (the item's accumulator buffer being
+    // free, then each stage's bytes) and hands the verdict over through bar.red, so
+    // the MMA warp touches neither an mbarrier nor shared memory between issues.
+    // Same item and stage sequence as the MMA warp, also after an abort, so that
+    // the named barrier (no time-out) always pairs.
+    int s = 0, buf = 0;
     uint32_t ph = 0;
+    uint32_t acc_ph[2] = {0, 0};
     Item it;
     for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it); i += stride) {
+      const bool item_ok =
+          __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(&tempty[buf], acc_ph[buf] ^ 1, abort_flag);
+      acc_ph[buf] ^= 1;
+      buf = (buf + 1 == p.acc_bufs) ? 0 : buf + 1;
       for (int kb = it.kb0; kb < it.kb1; ++kb) {
-        if (__all_sync(0xffffffffu, *abort_flag == 0)) mbar_wait_warp(&full[s], ph, abort_flag);
-        named_sync(kStreamHandoffBarrier, 64);
+        const bool ok =
+            item_ok && __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(&full[s], ph, abort_flag);
+        named_sync_and(kStreamHandoffBarrier, 64, ok);
         if (++s == STAGES) {
           s = 0;
           ph ^= 1;
@@ -243,32 +252,36 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     }
   } else if (warp == 1) {
     int s = 0, buf = 0;
-    uint32_t acc_ph[2] = {0, 0};
     Item it;
     for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it); i += stride) {
       const int n_mma = ((it.rows + 15) >> 4) * 16;
       const uint32_t idesc = idesc_nvf4(128, n_mma);
       const uint32_t acc = tmem + buf * p.acc_cols;
-      const bool item_ok =
-          __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(&tempty[buf], acc_ph[buf] ^ 1, abort_flag);
-      tc_fence_after();
+      bool item_ok = true;
       for (int kb = it.kb0; kb < it.kb1; ++kb) {
-        named_sync(kStreamHandoffBarrier, 64);  // the waiter saw this stage's bytes land
+        const bool ok = named_sync_and(kStreamHandoffBarrier, 64, true);
+        item_ok = item_ok && ok;
         tc_fence_after();
-        if (item_ok && __all_sync(0xffffffffu, *abort_flag == 0)) {
+        if (ok) {
           if (elect_one()) {
+            // Fully unrolled: a data-dependent trip count here makes the elected lane
+            // issue each tcgen05 instruction on its own, far more slowly.
             const int nsub = min(4, (K - kb * 256) / 64);
             const uint32_t w_addr = smem_u32(smem + s * L.stage_bytes);
             const uint32_t x_addr = w_addr + L.x_off;
             const uint32_t sf_col = sf_base + s * 32;
-            for (int kk = 0; kk < nsub; ++kk) {
-              tc_cp_32x128b_x4(sf_col + kk * 4, desc_sf(w_addr + L.sfw_off + kk * 512));
-              tc_cp_32x128b_x4(sf_col + 16 + kk * 4, desc_sf(w_addr + L.sfx_off + kk * 512));
-            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              if (kk < nsub) {
+                tc_cp_32x128b_x4(sf_col + kk * 4, desc_sf(w_addr + L.sfw_off + kk * 512));
+                tc_cp_32x128b_x4(sf_col + 16 + kk * 4, desc_sf(w_addr + L.sfx_off + kk * 512));
+              }
             const uint64_t wdesc = desc_sw128(w_addr), xdesc = desc_sw128(x_addr);
-            for (int kk = 0; kk < nsub; ++kk)
-              tc_mma_nvf4(acc, wdesc + 2 * kk, xdesc + 2 * kk, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4,
-                          (kb != it.kb0) || (kk != 0));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              if (kk < nsub)
+                tc_mma_nvf4(acc, wdesc + 2 * kk, xdesc + 2 * kk, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4,
+                            (kb != it.kb0) || (kk != 0));
             tc_commit(&empty[s]);
           }
           __syncwarp();
@@ -279,7 +292,6 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         if (elect_one()) tc_commit(&tfull[buf]);
         __syncwarp();
       }
-      acc_ph[buf] ^= 1;
       buf = (buf + 1 == p.acc_bufs) ? 0 : buf + 1;
     }
     if (p.pdl) griddep_launch_dependents();
