@@ -39,12 +39,12 @@ FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense ratio (fp4 13.5 PF vs bf16 2.25 PF)
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-breakdown", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--only", choices=["decode", "moe", "prefill"], default=None,
+    ap.add_argument("--only", choices=["square", "decode", "moe", "prefill"], default=None,
                     help="run only this breakdown workload (for profiling) and print its numbers")
     return ap.parse_args()
 
@@ -85,6 +85,68 @@ def load_peaks():
             pass
     return {"hbm": FALLBACK_HBM_GBS, "bf16": FALLBACK_BF16_TFLOPS, "bf16_sustained": 1700.0,
             "source": "fallback"}
+
+
+class NvmlSampler:
+    """SM clock and clock-event (throttle) reasons of this process's GPU, read through
+    NVML every 2 ms by a background thread while running (read-only queries)."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device):
+        import ctypes
+        import threading
+        self.ct, self.threading = ctypes, threading
+        self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nvml.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        import torch
+        props = torch.cuda.get_device_properties(torch_device)
+        ok = False
+        uuid = getattr(props, "uuid", None)
+        if uuid is not None:
+            ok = self.nvml.nvmlDeviceGetHandleByUUID(("GPU-" + str(uuid)).encode(), ctypes.byref(self.h)) == 0
+        if not ok and hasattr(props, "pci_bus_id"):
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+            ok = self.nvml.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) == 0
+        if not ok:
+            raise RuntimeError("no NVML handle for this device")
+        fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn if fn is not None else self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.samples, self.reason_bits, self.stop_flag, self.thread = [], 0, False, None
+
+    def _run(self):
+        ct = self.ct
+        mhz, bits = ct.c_uint(), ct.c_ulonglong()
+        while not self.stop_flag:
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) == 0:
+                self.samples.append(mhz.value)
+            if self.reasons_fn(self.h, ct.byref(bits)) == 0:
+                self.reason_bits |= bits.value
+            time.sleep(0.002)
+
+    def start(self):
+        self.thread = self.threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.stop_flag = True
+        self.thread.join()
+        smax = self.ct.c_uint()
+        self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, self.ct.byref(smax))
+        reasons = sorted(n for b, n in self.REASONS.items() if self.reason_bits & b)
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": smax.value or None, "reasons": reasons, "samples": len(self.samples),
+                "source": "nvml, 2 ms"}
+
+
+def clock_sampler(torch_device, index):
+    try:
+        return NvmlSampler(torch_device)
+    except Exception:
+        return ClockSampler(index)
 
 
 class ClockSampler:
@@ -246,7 +308,7 @@ def main():
     import synth
 
     dev = torch.device("cuda", local)
-    if args.only:
+    if args.only and args.only != "square":
         stream = torch.cuda.current_stream()
         peaks = load_peaks()
 
@@ -296,8 +358,7 @@ def main():
         m.nvfp4_gemm(a, sa, g1, b, sb, g2, SQ, SQ, SQ, y=y)
         return m.nvfp4_last_launch_count()
 
-    sampler = ClockSampler(local)
-    sampler.start()
+    sampler = clock_sampler(dev, local)
     for i in range(args.warmup):
         gemm(i)
     torch.cuda.synchronize()
@@ -308,6 +369,7 @@ def main():
     t_all0, t_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
     torch.cuda.synchronize()
+    sampler.start()
     t_all0.record(stream)
     for i in range(args.steps):
         starts[i].record(stream)
@@ -315,6 +377,7 @@ def main():
         ends[i].record(stream)
     t_all1.record(stream)
     torch.cuda.synchronize()
+    clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
     total_ms = t_all0.elapsed_time(t_all1)
@@ -322,6 +385,10 @@ def main():
     per_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
     ms_per_step = total_ms / args.steps
     value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    if args.only == "square":
+        print(json.dumps({"only": "square", "TFLOP/s": value, "per_launch_us": per_launch_ms * 1e3,
+                          "clocks": clocks}), flush=True)
+        return
 
     # ---- end to end through the C ABI with host buffers ------------------------------------
     host_in = [t.cpu().pin_memory() for t in sets[0][:6]]
@@ -349,7 +416,6 @@ def main():
     e2e_ms = reduce_max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = host_out.numel() * host_out.element_size()
-    clocks = sampler.stop()
 
     # ---- breakdown of the other workloads ---------------------------------------------------
     breakdown = {}
@@ -367,7 +433,7 @@ def main():
                    "l2": f"rotating {R} input/output sets ({R * op_bytes / 1e6:.0f} MB of operands > 129 MB L2)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
-                     "frac": achieved / fp4_peak, "traffic": profiled_traffic("k_gemm_dense"),
+                     "frac": achieved / fp4_peak, "traffic": profiled_traffic("k_gemm_dense_pair"),
                      "kernel": "k_gemm_dense_pair",
                      "peak_source": f"{peaks['source']} bf16 {peaks['bf16']:.0f} TFLOP/s x {FP4_OVER_BF16:g} (nominal fp4/bf16)"},
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

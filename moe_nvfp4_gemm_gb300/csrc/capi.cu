@@ -120,6 +120,20 @@ int encode_sf(CUtensorMap* m, const void* base, uint64_t chunks) {
   return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+// bf16 output [rows, cols] (cols contiguous) for TMA stores: boxes of 64 columns
+// (128 bytes, 128-byte swizzle) x 32 rows; elements outside the tensor are not written.
+int encode_out(CUtensorMap* m, void* base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return NVFP4_ERR_CUDA;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
 
 int64_t pad16(int64_t v) { return (v + 15) / 16 * 16; }
@@ -338,17 +352,18 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
   const int kernel = g_tune.dense_kernel ? g_tune.dense_kernel : 2;
   if (kernel == 2) {
     // CTA pairs, 256 x 256 tiles
-    CUtensorMap tmA, tmB, tmSFA, tmSFB;
+    CUtensorMap tmA, tmB, tmSFA, tmSFB, tmY;
     if ((rc = encode_2d(&tmA, a, M, K / 2, 128))) return rc;
     if ((rc = encode_2d(&tmB, b, N, K / 2, 128))) return rc;
     if ((rc = encode_sf(&tmSFA, sfa, nvfp4_scale_bytes(M, K) / 512))) return rc;
     if ((rc = encode_sf(&tmSFB, sfb, nvfp4_scale_bytes(N, K) / 512))) return rc;
+    if ((rc = encode_out(&tmY, y, M, N))) return rc;
     DenseArgs da = {sfa, sfb, ga, gb, y, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), dev_status};
     const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
     int pairs = (g_tune.dense_grid ? g_tune.dense_grid : d.sms) / 2;
     if (pairs > tiles) pairs = static_cast<int>(tiles);
     if (pairs < 1) pairs = 1;
-    rc = from_cuda(launch_dense_pair(tmA, tmB, tmSFA, tmSFB, da, 2 * pairs, st));
+    rc = from_cuda(launch_dense_pair(tmA, tmB, tmSFA, tmSFB, tmY, da, 2 * pairs, st));
     g_last_launches = 1;
     return rc;
   }

@@ -228,20 +228,23 @@ struct PairCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int SF_COLS = 16 + 32;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int OUT_BYTES = 8 * 4096;  // one 32 x 64 bf16 store box per epilogue warp
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_BYTES + 1024 + 256;
   static_assert(256 + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(STAGE_BYTES % 1024 == 0, "swizzled buffers stay 1024-byte aligned");
 };
 
 __global__ void __launch_bounds__(kPairThreads, 1)
     k_gemm_dense_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                      const DenseArgs p) {
+                      const __grid_constant__ CUtensorMap tmY, const DenseArgs p) {
   using C = PairCfg;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint8_t* out_buf = smem + STAGES * C::STAGE_BYTES;  // 1024-byte aligned: STAGE_BYTES is a multiple of 1024
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_buf + C::OUT_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 1;
@@ -266,6 +269,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmSFA);
     prefetch_tmap(&tmSFB);
+    prefetch_tmap(&tmY);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
@@ -397,21 +401,22 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   } else {
     const int q = warp & 3, h = (warp - 2) >> 2;
     const float alpha = __ldg(p.ga) * __ldg(p.gb);
-    const bool wide = N % 16 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 31) == 0;
+    uint8_t* buf = out_buf + (warp - 2) * 4096;
     const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
     uint32_t acc_ph = 0;
     for (int t = pair; t < tiles; t += npairs) {
       const int m_blk = t % mt, n_blk = t / mt;
       if (!mbar_wait_warp(tfull, acc_ph, abort_flag)) break;
       tc_fence_after();
-      const int row = m_blk * 256 + rank * 128 + q * 32 + lane;
-      drain_accumulator<128>(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128, alpha,
-                             p.y + static_cast<int64_t>(row) * N, row < M, n_blk * 256 + h * 128, N, wide, [&] {
-                               if (elect_one()) mbar_arrive_cluster(tempty_leader);
-                               __syncwarp();
-                             });
+      drain_accumulator_tma<128>(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128, alpha, buf, &tmY,
+                                 n_blk * 256 + h * 128, m_blk * 256 + rank * 128 + q * 32, [&] {
+                                   if (elect_one()) mbar_arrive_cluster(tempty_leader);
+                                   __syncwarp();
+                                 });
       acc_ph ^= 1;
     }
+    if (lane == 0) bulk_wait_group0();  // this warp's stores are complete before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -445,7 +450,8 @@ cudaError_t launch_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const D
 
 // grid: an even number of CTAs (two per 256 x 256 tile in flight).
 cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
-                              const CUtensorMap& tmSFB, const DenseArgs& a, int grid, cudaStream_t st) {
+                              const CUtensorMap& tmSFB, const CUtensorMap& tmY, const DenseArgs& a, int grid,
+                              cudaStream_t st) {
   cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_gemm_dense_pair));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -460,7 +466,7 @@ cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, co
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k_gemm_dense_pair, tmA, tmB, tmSFA, tmSFB, a);
+  e = cudaLaunchKernelEx(&cfg, k_gemm_dense_pair, tmA, tmB, tmSFA, tmSFB, tmY, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

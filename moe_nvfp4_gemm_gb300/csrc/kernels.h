@@ -49,7 +49,8 @@ cudaError_t launch_encode(int which, const float* v, int64_t n, uint8_t* out, cu
 cudaError_t launch_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const DenseArgs& a, int bn, int grid,
                          cudaStream_t st);
 cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
-                              const CUtensorMap& tmSFB, const DenseArgs& a, int grid, cudaStream_t st);
+                              const CUtensorMap& tmSFB, const CUtensorMap& tmY, const DenseArgs& a, int grid,
+                              cudaStream_t st);
 cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, bool grouped,
                           int grid, cudaStream_t st);
 cudaError_t launch_grouped_prep(const int32_t* offsets, int E, int M_total, int K, const uint8_t* sfx,

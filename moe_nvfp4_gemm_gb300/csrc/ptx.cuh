@@ -148,6 +148,23 @@ DEVI void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t x,
       : "memory");
 }
 
+// 2-D tiled TMA store shared -> global, tracked by this thread's bulk async-group.
+// Elements of the box outside the tensor are not written.
+DEVI void tma_store_2d(const CUtensorMap* m, const void* src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+DEVI void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until this thread's bulk stores have finished reading shared memory.
+DEVI void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Waits until this thread's bulk stores are complete.
+DEVI void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy
+// (TMA) reads of them.
+DEVI void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Plain bulk copy global -> shared; both addresses 16-byte aligned, bytes % 16 == 0.
 DEVI void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
   asm volatile(
@@ -390,6 +407,51 @@ DEVI void drain_accumulator(uint32_t taddr, float alpha, uint16_t* yrow, bool ro
         if (col0 + c < N) st_global_v4(yrow + col0 + c, w[0], w[1], w[2], w[3]);
         if (col0 + c + 8 < N) st_global_v4(yrow + col0 + c + 8, w[4], w[5], w[6], w[7]);
       }
+    }
+  }
+}
+
+// As drain_accumulator, but the bf16 rows leave through TMA stores: the warp
+// writes each 32-row x 64-column block into its 4 KB shared-memory buffer `buf`
+// (1024-byte aligned, 128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8),
+// which keeps the 32 lanes' writes at 4 wavefronts) and lane 0 stores it to
+// y[row0 .. row0 + 32) x [col0 + 64 j ..) through tmY (box 64 x 32, clipped at the
+// tensor's edges). The stores leave the load/store unit free and write whole
+// 128-byte lines, so they do not compete with the TMA operand loads the way 32
+// rows of scattered sector writes per instruction do.
+template <int NC, typename Release>
+DEVI void drain_accumulator_tma(uint32_t taddr, float alpha, uint8_t* buf, const CUtensorMap* tmY, int col0, int row0,
+                                Release release) {
+  static_assert(NC % 64 == 0, "64-column store boxes");
+  const int lane = threadIdx.x & 31;
+  uint32_t r[NC];
+#pragma unroll
+  for (int c = 0; c < NC; c += 32) tmem_ld32(taddr + c, r + c);
+  tmem_ld_wait();
+  tc_fence_before();
+  __syncwarp();
+  release();
+  const uint32_t row_addr = smem_u32(buf) + lane * 128;
+#pragma unroll
+  for (int j = 0; j < NC / 64; ++j) {
+    if (lane == 0) bulk_wait_group_read0();  // the previous box has left the buffer
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t* v = r + j * 64 + c * 8;
+      const uint32_t a = row_addr + ((c ^ (lane & 7)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                   "r"(pack_bf16x2(__uint_as_float(v[0]) * alpha, __uint_as_float(v[1]) * alpha)),
+                   "r"(pack_bf16x2(__uint_as_float(v[2]) * alpha, __uint_as_float(v[3]) * alpha)),
+                   "r"(pack_bf16x2(__uint_as_float(v[4]) * alpha, __uint_as_float(v[5]) * alpha)),
+                   "r"(pack_bf16x2(__uint_as_float(v[6]) * alpha, __uint_as_float(v[7]) * alpha))
+                   : "memory");
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmY, buf, col0 + j * 64, row0);
+      bulk_commit_group();
     }
   }
 }
