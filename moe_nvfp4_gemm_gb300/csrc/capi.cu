@@ -331,16 +331,17 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
     s.split = split;
     s.pdl = g_tune.pdl;
     const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0) - 1536;
+    const int recv_bytes = stream_recv_bytes(s.M, split);
     int stages = g_tune.stream_stages;
     if (stages == 0) {
-      stages = (110 * 1024 - 1536) / stage_bytes;  // two CTAs per SM
+      stages = (110 * 1024 - 1536 - recv_bytes) / stage_bytes;  // two CTAs per SM
       const int tmem_room = (256 - s.acc_cols) / 32;
       if (stages > tmem_room) stages = tmem_room;
       if (stages < 2) stages = 2;
     }
-    // the split-K partials (M x 128 fp32) reuse the stage ring
-    while (split > 1 && stages * stage_bytes < s.M * 512) ++stages;
-    if (stream_smem_bytes(stages, s.x_rows, 0) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    // the outgoing split-K partials (split x ceil(M / split) x 128 fp32) reuse the stage ring
+    while (split > 1 && stages * stage_bytes < recv_bytes) ++stages;
+    if (stream_smem_bytes(stages, s.x_rows, recv_bytes) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     s.stages = stages;
     s.tmem_cols = pow2_at_least(s.acc_cols + 32 * stages);
     if (s.tmem_cols > 512) return NVFP4_ERR_UNSUPPORTED_SHAPE;

@@ -35,22 +35,10 @@ struct StreamLayout {
   }
 };
 
-DEVI void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 DEVI uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
-}
-
-DEVI float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
-  uint32_t remote;
-  float v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
 }
 
 struct Item {
@@ -82,8 +70,10 @@ DEVI bool get_item(const StreamArgs& p, int i, int n_items, int NT, int KB, Item
     it.row0 = 0;
     it.rows = p.M;
     it.slab = 0;
-    it.kb0 = static_cast<int>((static_cast<int64_t>(KB) * sp) / p.split);
-    it.kb1 = static_cast<int>((static_cast<int64_t>(KB) * (sp + 1)) / p.split);
+    // 32-bit arithmetic (KB * split <= 2^23 * 8 for every accepted K): a 64-bit division
+    // costs the producer ~0.3 us on its way to the first load
+    it.kb0 = (KB * sp) / p.split;
+    it.kb1 = (KB * (sp + 1)) / p.split;
   }
   return true;
 }
@@ -94,6 +84,7 @@ DEVI bool get_item(const StreamArgs& p, int i, int n_items, int NT, int KB, Item
 constexpr int kStreamThreads = 224;
 constexpr int kStreamWaiterWarp = 6;
 constexpr uint32_t kStreamHandoffBarrier = 1;
+constexpr uint32_t kStreamEpilogueBarrier = 2;  // the 4 epilogue warps
 
 template <bool GROUPED>
 __global__ void __launch_bounds__(kStreamThreads, 2)
@@ -103,19 +94,30 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const StreamLayout L(p.x_rows);
   const int STAGES = p.stages;
-  // split-K partial sums of this CTA [token][128 rows] fp32: the stage ring is reused
-  // (one item per CTA; every stage has been consumed when the epilogue runs)
+  // Split-K (dense, S = p.split > 1): CTA rank r of a cluster owns tokens
+  // [r * m_own, (r + 1) * m_own). Its partial sums leave from `part` = [token][128 rows]
+  // fp32, which reuses the stage ring (one item per CTA; every stage has been consumed
+  // when the epilogue runs), so each owner's block is contiguous, and arrive in the
+  // owner's `recv` = [source rank][token - r * m_own][128].
+  const int S = GROUPED ? 1 : p.split;
+  const int m_own = (p.M + S - 1) / S;  // token slots per owner
   float* part = reinterpret_cast<float*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * L.stage_bytes);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;  // [2]
   uint64_t* tempty = tfull + 2;      // [2]
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* red_bar = drain + 1;     // all S partials of this CTA's tokens have landed
+  volatile uint64_t* policies = red_bar + 1;  // [2] L2 cache policies (weights, tokens) once published
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_bar + 3);
+  volatile uint32_t* policies_ready = tmem_slot + 2;
+  float* recv = reinterpret_cast<float*>(smem + STAGES * L.stage_bytes + 512);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
+    prefetch_tmap(&tmW);  // first, so that the descriptors are fetched while the barriers are set up
+    prefetch_tmap(&tmX);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
@@ -125,10 +127,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
       mbar_init(&tempty[b], 4);  // one elected lane per epilogue warp
     }
     mbar_init(drain, 1);
+    mbar_init(red_bar, 1);
     *abort_flag = 0;
+    *policies_ready = 0;
     fence_mbar_init();
-    prefetch_tmap(&tmW);
-    prefetch_tmap(&tmX);
+    if (S > 1) {
+      const int mine = min(m_own, p.M - static_cast<int>(cluster_rank()) * m_own);  // tokens this CTA owns
+      if (mine > 0) mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>(S * mine * 512));
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, p.tmem_cols);
@@ -138,6 +144,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Every CTA's reduction barrier is initialised (published by thread 0's
+  // fence.mbarrier_init.release.cluster) before any CTA of the cluster sends partials;
+  // only the sending warp waits, at the very end. The arrive itself is relaxed: a
+  // release at cluster scope would hold the producer's first loads for ~1 us.
+  if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   const int N = p.N, K = p.K;
   const int NT = (N + 127) / 128;
@@ -160,7 +171,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   const uint32_t sf_base = tmem + p.acc_bufs * p.acc_cols;
 
   if (warp == 0) {
-    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+    // The first ring goes out without L2 hints; createpolicy costs ~0.6 us, so an idle
+    // epilogue warp builds the policies and the producer picks them up once published.
+    uint64_t pol_w = 0, pol_x = 0;
+    bool have_pol = false;
+    int issued = 0;
     int s = 0;
     uint32_t ph = 0;
     int issued_phase[16];
@@ -178,16 +193,36 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
       const uint8_t* sfx = p.sfx + static_cast<int64_t>(it.slab) * KC4 * 512;
       for (int kb = it.kb0; kb < it.kb1; ++kb) {
         if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag)) break;
+        if (!have_pol && issued >= STAGES && *policies_ready) {
+          __threadfence_block();
+          pol_w = policies[0];
+          pol_x = policies[1];
+          have_pol = true;
+        }
+        const bool hint = have_pol;
+        ++issued;
         if (elect_one()) {
           const int nsub = min(4, (K - kb * 256) / 64);
           uint8_t* st = smem + s * L.stage_bytes;
           mbar_arrive_expect_tx(&full[s], 16384 + n16 * 2048 + nsub * 1024);
-          tma_load_2d(st, &tmW, &full[s], kb * 128, static_cast<int32_t>(wrow0), pol_w);
-          bulk_load(st + L.sfw_off, sfw + kb * 2048, nsub * 512, &full[s], pol_w);
+          if (hint) {
+            tma_load_2d(st, &tmW, &full[s], kb * 128, static_cast<int32_t>(wrow0), pol_w);
+            bulk_load(st + L.sfw_off, sfw + kb * 2048, nsub * 512, &full[s], pol_w);
+          } else {
+            tma_load_2d_plain(st, &tmW, &full[s], kb * 128, static_cast<int32_t>(wrow0));
+            bulk_load_plain(st + L.sfw_off, sfw + kb * 2048, nsub * 512, &full[s]);
+          }
           if (!pending) {
-            for (int j = 0; j < n16; ++j)
-              tma_load_2d(st + L.x_off + j * 2048, &tmX, &full[s], kb * 128, it.row0 + j * 16, pol_x);
-            bulk_load(st + L.sfx_off, sfx + kb * 2048, nsub * 512, &full[s], pol_x);
+            for (int j = 0; j < n16; ++j) {
+              if (hint)
+                tma_load_2d(st + L.x_off + j * 2048, &tmX, &full[s], kb * 128, it.row0 + j * 16, pol_x);
+              else
+                tma_load_2d_plain(st + L.x_off + j * 2048, &tmX, &full[s], kb * 128, it.row0 + j * 16);
+            }
+            if (hint)
+              bulk_load(st + L.sfx_off, sfx + kb * 2048, nsub * 512, &full[s], pol_x);
+            else
+              bulk_load_plain(st + L.sfx_off, sfx + kb * 2048, nsub * 512, &full[s]);
           }
         }
         __syncwarp();
@@ -209,9 +244,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
               const int nsub = min(4, (K - kbj * 256) / 64);
               uint8_t* st = smem + pend_stage[j] * L.stage_bytes;
               for (int r = 0; r < n16; ++r)
-                tma_load_2d(st + L.x_off + r * 2048, &tmX, &full[pend_stage[j]], kbj * 128, it.row0 + r * 16,
-                            pol_x);
-              bulk_load(st + L.sfx_off, sfx + kbj * 2048, nsub * 512, &full[pend_stage[j]], pol_x);
+                tma_load_2d_plain(st + L.x_off + r * 2048, &tmX, &full[pend_stage[j]], kbj * 128, it.row0 + r * 16);
+              bulk_load_plain(st + L.sfx_off, sfx + kbj * 2048, nsub * 512, &full[pend_stage[j]]);
             }
           }
           __syncwarp();
@@ -301,6 +335,16 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     mbar_wait_warp(drain, 0, &dummy);
   } else {
     constexpr int MAXC = kGroupTile;
+    if (warp == 2) {
+      const uint64_t pw = policy_evict_first(), px = policy_evict_last();
+      if (lane == 0) {
+        policies[0] = pw;
+        policies[1] = px;
+        __threadfence_block();
+        *policies_ready = 1;
+      }
+      __syncwarp();
+    }
     if (!GROUPED && p.pdl) griddep_wait();  // the global scales may come from the previous kernel
     const int q = warp & 3;
     const float ga = __ldg(p.ga);
@@ -344,7 +388,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
           for (int j = 0; j < 32; ++j) {
             const int tok = c + j;
             if (tok < it.rows) {
-              if (p.split > 1)
+              if (S > 1)
                 part[tok * 128 + q * 32 + lane] = has_k ? __uint_as_float(r[j]) : 0.0f;
               else if (wrow < N)
                 p.y[static_cast<int64_t>(it.row0 + tok) * N + wrow] =
@@ -363,28 +407,47 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     if (p.pdl) griddep_launch_dependents();
   }
 
-  if (!GROUPED && p.split > 1) {
-    // Sum the S partial tiles of this cluster through distributed shared memory, in
-    // rank order; CTA rank r finishes tokens r, r + S, ... A second barrier keeps every
-    // CTA's partials alive until they have been read. (Issuing all remote loads before
-    // summing measured ~3 us slower per call than this loop.)
-    cluster_sync_all();
-    if (warp >= 2 && warp < kStreamWaiterWarp) {
+  if (!GROUPED && S > 1 && warp >= 2 && warp < kStreamWaiterWarp) {
+    // One-way split-K reduction: each CTA sends owner o the block of o's tokens
+    // (one bulk copy into o's recv slot for this rank, completing bytes on o's
+    // red_bar), then the owners sum their S slots locally. No cluster-wide barrier
+    // sits between the last MMA and the stores.
+    fence_proxy_async_shared();  // this thread's part[] writes, before the bulk copies read them
+    named_sync(kStreamEpilogueBarrier, 128);
+    const uint32_t rank = cluster_rank();
+    if (warp == 2) {
+      asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+      if (lane == 0) {
+        for (int o = 0; o < S; ++o) {
+          const int n_o = min(m_own, p.M - o * m_own);
+          if (n_o <= 0) continue;
+          const uint32_t dst = mapa_shared(smem_u32(recv + static_cast<int>(rank) * m_own * 128), o);
+          bulk_copy_to_cluster(dst, part + o * m_own * 128, static_cast<uint32_t>(n_o * 512),
+                               mapa_shared(smem_u32(red_bar), o));
+        }
+        bulk_commit_group();
+        bulk_wait_group_read0();  // part[] may be released once the copies have read it
+      }
+      __syncwarp();
+    }
+    const int mine = min(m_own, p.M - static_cast<int>(rank) * m_own);
+    if (mine > 0 && mbar_wait_warp(red_bar, 0, abort_flag)) {
       const int q = warp & 3;
-      const uint32_t rank = cluster_rank();
-      const int wt = blockIdx.x / p.split;
-      const int wrow = wt * 128 + q * 32 + lane;
+      const int wrow = (blockIdx.x / S) * 128 + q * 32 + lane;
       const float alpha = __ldg(p.ga) * __ldg(p.gb);
-      const uint32_t red_addr = smem_u32(part);
-      for (int tok = rank; tok < p.M; tok += p.split) {
+      for (int idx = 0; idx < mine; ++idx) {
         float v = 0.0f;
-        for (int c = 0; c < p.split; ++c) v += ld_dsmem_f32(red_addr + (tok * 128 + q * 32 + lane) * 4, c);
+        for (int c = 0; c < S; ++c) v += recv[(c * m_own + idx) * 128 + q * 32 + lane];  // fixed rank order
+        const int tok = static_cast<int>(rank) * m_own + idx;
         if (wrow < N) p.y[static_cast<int64_t>(tok) * N + wrow] = __bfloat16_as_ushort(__float2bfloat16_rn(v * alpha));
       }
     }
-    cluster_sync_all();
   }
 
+  // Every thread that arrived on the cluster barrier also waits on it before the
+  // CTA-wide barrier below (the sending warp already did). Leaving arrivals without a
+  // wait let the __syncthreads that follows complete before all warps reached it.
+  if (S > 1 && !(warp == 2)) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -468,8 +531,7 @@ __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict_
 template <bool GROUPED>
 static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, int grid,
                                    cudaStream_t st) {
-  const StreamLayout L(a.x_rows);
-  const int smem = a.stages * L.stage_bytes + 1024 + 512;
+  const int smem = stream_smem_bytes(a.stages, a.x_rows, GROUPED ? 0 : stream_recv_bytes(a.M, a.split));
   cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_gemm_stream<GROUPED>));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -497,6 +559,9 @@ static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tm
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
+
+// Receive area of the one-way split-K reduction: S slots of ceil(M / S) tokens x 128 fp32.
+int stream_recv_bytes(int M, int split) { return split > 1 ? split * ((M + split - 1) / split) * 512 : 0; }
 
 int stream_smem_bytes(int stages, int x_rows, int recv_bytes) {
   return stages * StreamLayout(x_rows).stage_bytes + recv_bytes + 1024 + 512;

@@ -57,6 +57,7 @@ cudaError_t launch_grouped_prep(const int32_t* offsets, int E, int M_total, int 
                                 int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
                                 cudaStream_t st);
 int stream_smem_bytes(int stages, int x_rows, int recv_bytes);
+int stream_recv_bytes(int M, int split);
 
 // Raises `func`'s dynamic shared-memory limit to the opt-in maximum, once per
 // (kernel, device); later calls only look the pair up.

@@ -165,6 +165,32 @@ DEVI void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "m
 // (TMA) reads of them.
 DEVI void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// The same loads without an L2 cache hint: createpolicy costs the issuing warp about
+// a microsecond, so latency-bound kernels issue their first ring without one.
+DEVI void tma_load_2d_plain(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+DEVI void bulk_load_plain(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Bulk copy from this CTA's shared memory into another CTA's of the cluster, completing
+// `bytes` on the mbarrier at `bar_cluster` there; tracked by this thread's bulk group.
+DEVI void bulk_copy_to_cluster(uint32_t dst_cluster, const void* src, uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
 // Plain bulk copy global -> shared; both addresses 16-byte aligned, bytes % 16 == 0.
 DEVI void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
   asm volatile(
