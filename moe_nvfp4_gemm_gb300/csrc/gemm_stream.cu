@@ -115,6 +115,70 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = p.N, K = p.K;
+  const int NT = (N + 127) / 128;
+  const int KB = (K + 255) / 256;
+  const int64_t KC4 = K / 64;
+
+  // Where an item's tiles come from (computed once per item).
+  struct Src {
+    int32_t wrow0, row0;
+    int n16;
+    const uint8_t* sfw;
+    const uint8_t* sfx;
+  };
+  auto item_src = [&](const Item& it) {
+    Src r;
+    r.wrow0 = it.e * N + it.wt * 128;
+    r.row0 = it.row0;
+    r.n16 = (it.rows + 15) >> 4;
+    r.sfw = p.sfw + it.e * p.sfw_stride + static_cast<int64_t>(it.wt) * KC4 * 512;
+    r.sfx = p.sfx + static_cast<int64_t>(it.slab) * KC4 * 512;
+    return r;
+  };
+  // Requests stage st_idx = K block kb of an item: the 128-row weight tile and its
+  // scales, and unless deferred (with_x false) the token tile and its scales.
+  auto issue_stage = [&](int st_idx, int kb, const Src& src, bool with_x, bool hint, uint64_t pol_w,
+                         uint64_t pol_x) {
+    const int n16 = src.n16;
+    const int32_t wrow0 = src.wrow0;
+    const uint8_t* sfw = src.sfw;
+    const uint8_t* sfx = src.sfx;
+    const int nsub = min(4, (K - kb * 256) / 64);
+    uint8_t* st = smem + st_idx * L.stage_bytes;
+    uint64_t* bar = &full[st_idx];
+    mbar_arrive_expect_tx(bar, 16384 + n16 * 2048 + nsub * 1024);
+    if (hint) {
+      tma_load_2d(st, &tmW, bar, kb * 128, wrow0, pol_w);
+      bulk_load(st + L.sfw_off, sfw + kb * 2048, nsub * 512, bar, pol_w);
+    } else {
+      tma_load_2d_plain(st, &tmW, bar, kb * 128, wrow0);
+      bulk_load_plain(st + L.sfw_off, sfw + kb * 2048, nsub * 512, bar);
+    }
+    if (with_x) {
+      for (int j = 0; j < n16; ++j) {
+        if (hint)
+          tma_load_2d(st + L.x_off + j * 2048, &tmX, bar, kb * 128, src.row0 + j * 16, pol_x);
+        else
+          tma_load_2d_plain(st + L.x_off + j * 2048, &tmX, bar, kb * 128, src.row0 + j * 16);
+      }
+      if (hint)
+        bulk_load(st + L.sfx_off, sfx + kb * 2048, nsub * 512, bar, pol_x);
+      else
+        bulk_load_plain(st + L.sfx_off, sfx + kb * 2048, nsub * 512, bar);
+    }
+  };
+  // Dense path: the first ring of this CTA's (single) item is requested by thread 0
+  // straight after the barriers exist, ahead of TMEM allocation and the CTA-wide
+  // barrier; under a programmatic dependency only the weights (the token tiles may
+  // come from the previous kernel).
+  Item first_it;
+  int n_pre = 0;
+  if (!GROUPED) {
+    get_item<false>(p, blockIdx.x, NT * p.split, NT, KB, first_it);
+    n_pre = min(STAGES, first_it.kb1 - first_it.kb0);
+  }
+
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmW);  // first, so that the descriptors are fetched while the barriers are set up
     prefetch_tmap(&tmX);
@@ -135,6 +199,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
       const int mine = min(m_own, p.M - static_cast<int>(cluster_rank()) * m_own);  // tokens this CTA owns
       if (mine > 0) mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>(S * mine * 512));
     }
+    const Src src = item_src(first_it);
+    for (int j = 0; j < n_pre; ++j) issue_stage(j, first_it.kb0 + j, src, !p.pdl, false, 0, 0);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, p.tmem_cols);
@@ -149,11 +215,6 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   // only the sending warp waits, at the very end. The arrive itself is relaxed: a
   // release at cluster scope would hold the producer's first loads for ~1 us.
   if (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-
-  const int N = p.N, K = p.K;
-  const int NT = (N + 127) / 128;
-  const int KB = (K + 255) / 256;
-  const int64_t KC4 = K / 64;
   // With a programmatic dependency the prologue above overlapped the previous kernel.
   // The grouped path reads the tile list the preparation kernel just wrote, so every
   // warp waits here; the dense path's producer first requests its first weight tiles.
@@ -170,6 +231,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   }
   const uint32_t sf_base = tmem + p.acc_bufs * p.acc_cols;
 
+  float dense_alpha = 0.0f;  // epilogue warps: g_a * g_b of the dense path
   if (warp == 0) {
     // The first ring goes out without L2 hints; createpolicy costs ~0.6 us, so an idle
     // epilogue warp builds the policies and the producer picks them up once published.
@@ -187,10 +249,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     int pend_stage[16], pend_kb[16], npend = 0;
     Item it;
     for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it) && !*abort_flag; i += stride) {
-      const int n16 = (it.rows + 15) >> 4;
-      const int64_t wrow0 = static_cast<int64_t>(it.e) * N + it.wt * 128;
-      const uint8_t* sfw = p.sfw + it.e * p.sfw_stride + static_cast<int64_t>(it.wt) * KC4 * 512;
-      const uint8_t* sfx = p.sfx + static_cast<int64_t>(it.slab) * KC4 * 512;
+      const Src src = item_src(it);
+      const int n16 = src.n16;
+      const uint8_t* sfx = src.sfx;
       for (int kb = it.kb0; kb < it.kb1; ++kb) {
         if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag)) break;
         if (!have_pol && issued >= STAGES && *policies_ready) {
@@ -199,32 +260,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
           pol_x = policies[1];
           have_pol = true;
         }
-        const bool hint = have_pol;
+        const bool pre = issued < n_pre;  // requested in the prologue
         ++issued;
-        if (elect_one()) {
-          const int nsub = min(4, (K - kb * 256) / 64);
-          uint8_t* st = smem + s * L.stage_bytes;
-          mbar_arrive_expect_tx(&full[s], 16384 + n16 * 2048 + nsub * 1024);
-          if (hint) {
-            tma_load_2d(st, &tmW, &full[s], kb * 128, static_cast<int32_t>(wrow0), pol_w);
-            bulk_load(st + L.sfw_off, sfw + kb * 2048, nsub * 512, &full[s], pol_w);
-          } else {
-            tma_load_2d_plain(st, &tmW, &full[s], kb * 128, static_cast<int32_t>(wrow0));
-            bulk_load_plain(st + L.sfw_off, sfw + kb * 2048, nsub * 512, &full[s]);
-          }
-          if (!pending) {
-            for (int j = 0; j < n16; ++j) {
-              if (hint)
-                tma_load_2d(st + L.x_off + j * 2048, &tmX, &full[s], kb * 128, it.row0 + j * 16, pol_x);
-              else
-                tma_load_2d_plain(st + L.x_off + j * 2048, &tmX, &full[s], kb * 128, it.row0 + j * 16);
-            }
-            if (hint)
-              bulk_load(st + L.sfx_off, sfx + kb * 2048, nsub * 512, &full[s], pol_x);
-            else
-              bulk_load_plain(st + L.sfx_off, sfx + kb * 2048, nsub * 512, &full[s]);
-          }
-        }
+        if (!pre && elect_one()) issue_stage(s, kb, src, !pending, have_pol, pol_w, pol_x);
         __syncwarp();
         if (pending) {
           pend_stage[npend] = s;
@@ -348,13 +386,15 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     if (!GROUPED && p.pdl) griddep_wait();  // the global scales may come from the previous kernel
     const int q = warp & 3;
     const float ga = __ldg(p.ga);
+    const float gb0 = GROUPED ? 0.0f : __ldg(p.gb);  // dense: read while the mainloop runs
+    dense_alpha = ga * gb0;
     int buf = 0;
     uint32_t acc_ph[2] = {0, 0};
     Item it;
     for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it); i += stride) {
       if (!mbar_wait_warp(&tfull[buf], acc_ph[buf], abort_flag)) break;
       tc_fence_after();
-      const float alpha = ga * __ldg(p.gb + it.e);
+      const float alpha = ga * (GROUPED ? __ldg(p.gb + it.e) : gb0);
       const int wrow = it.wt * 128 + q * 32 + lane;  // output column
       const int n_mma = ((it.rows + 15) >> 4) * 16;
       const bool has_k = it.kb1 > it.kb0;
@@ -434,7 +474,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     if (mine > 0 && mbar_wait_warp(red_bar, 0, abort_flag)) {
       const int q = warp & 3;
       const int wrow = (blockIdx.x / S) * 128 + q * 32 + lane;
-      const float alpha = __ldg(p.ga) * __ldg(p.gb);
+      const float alpha = dense_alpha;
       for (int idx = 0; idx < mine; ++idx) {
         float v = 0.0f;
         for (int c = 0; c < S; ++c) v += recv[(c * m_own + idx) * 128 + q * 32 + lane];  // fixed rank order
