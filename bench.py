@@ -202,24 +202,32 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def csrc_hash():
+# Sources each profiled kernel is built from: a recorded DRAM traffic figure stays valid
+# only while these files are unchanged.
+KERNEL_SOURCES = {
+    "k_gemm_dense_pair": ["gemm_dense.cu", "ptx.cuh", "kernels.h"],
+}
+
+
+def kernel_src_hash(kernel: str):
     h = hashlib.sha256()
     d = os.path.join(ROOT, "moe_nvfp4_gemm_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in sorted(KERNEL_SOURCES[kernel]):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if taken on this source."""
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json), if it
+    was taken on the kernel's current sources; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     ent = d.get(kernel)
-    if not ent or ent.get("csrc_hash") != csrc_hash():
+    if not ent or ent.get("src_hash") != kernel_src_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 

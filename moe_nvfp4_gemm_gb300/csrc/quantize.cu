@@ -97,17 +97,59 @@ __global__ void __launch_bounds__(256) k_amax_final(const float* __restrict__ pa
 
 constexpr int kQuantTiles = 4;  // 512-byte scale tiles (128 rows x 64 columns) per CTA
 
-DEVI void quantize_block(const uint32_t (&w)[8], float g, uint32_t& s, uint2& packed_out) {
-  float f[16];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    f[2 * j] = bf16lo(w[j]);
-    f[2 * j + 1] = bf16hi(w[j]);
-  }
+// Packed pair of fp32 (Blackwell's f32x2 datapath: two IEEE round-to-nearest
+// operations per instruction, lane by lane).
+DEVI uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+DEVI void f2_split(uint64_t v, float& lo, float& hi) { asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v)); }
+DEVI uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+DEVI uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// v with the sign bit of x: the quotient of a nonzero x already has x's sign, and a
+// zero x (either sign) must keep its own (the correction step below yields +0 for -0).
+DEVI float with_sign_of(float v, float x) {
+  return __uint_as_float((__float_as_uint(v) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+}
+// Eight E2M1 codes, element 2j in the low nibble of byte j.
+DEVI uint32_t e2m1x8_encode(const float (&v)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
+// RN(x / d) given y = RN(1 / d): one Markstein correction of RN(x y), exact when x, d
+// and the quotient stay well inside the normal range; otherwise the IEEE division.
+DEVI float div_rn_by(float x, float d, float y) {
+  const float ax = fabsf(x);
+  if (ax < 1e-30f || ax > 1e30f || d < 1e-30f || d > 1e30f) return __fdiv_rn(x, d);
+  const float q0 = __fmul_rn(x, y);
+  return __fmaf_rn(__fmaf_rn(-q0, d, x), y, q0);
+}
+
+// g_inv = RN(1 / g), computed once per thread.
+DEVI void quantize_block(const uint32_t (&w)[8], float g, float g_inv, uint32_t& s, uint2& packed_out) {
   float amax = 0.0f;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
-  const float t = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
+  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(w[j])), fabsf(bf16hi(w[j]))));
+  // RN(RN(amax / 6) / g); 0x3e2aaaab = RN(1 / 6)
+  const float t = amax == 0.0f ? 0.0f : div_rn_by(div_rn_by(amax, 6.0f, __uint_as_float(0x3e2aaaabu)), g, g_inv);
   s = e4m3_encode(t);
   uint32_t packed[2] = {0u, 0u};
   if (s != 0) {
@@ -115,26 +157,29 @@ DEVI void quantize_block(const uint32_t (&w)[8], float g, uint32_t& s, uint2& pa
     // x / d correctly rounded without a division per element: y = RN(1/d), q0 = RN(x y)
     // is within one ulp of x / d, the remainder x - q0 d is exact (fma), and
     // RN(q0 + rem * y) = RN(x / d) by Markstein's theorem when nothing over- or
-    // underflows. Blocks outside that range take IEEE division; exact zeros keep
-    // their sign.
+    // underflows. Blocks outside that range take IEEE division.
     const float y = __frcp_rn(d);
     const bool fast = d > 1e-30f && d < 1e30f && __fmul_rn(amax, y) < 1e30f;
+    const uint64_t yy = f2(y, y), nd = f2(-d, -d);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float v[2];
+    for (int h = 0; h < 2; ++h) {  // eight elements (one output word) at a time
+      float v[8];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float x = f[2 * j + h];
+      for (int jj = 0; jj < 4; ++jj) {
+        const float lo = bf16lo(w[h * 4 + jj]), hi = bf16hi(w[h * 4 + jj]);
         if (fast) {
-          const float q0 = __fmul_rn(x, y);
-          const float r = __fmaf_rn(-q0, d, x);
-          v[h] = (x == 0.0f) ? x : __fmaf_rn(r, y, q0);
+          const uint64_t xx = f2(lo, hi);
+          const uint64_t q0 = f2_mul(xx, yy);
+          const uint64_t rem = f2_fma(q0, nd, xx);  // x - q0 d, exact
+          f2_split(f2_fma(rem, yy, q0), v[2 * jj], v[2 * jj + 1]);
+          v[2 * jj] = with_sign_of(v[2 * jj], lo);
+          v[2 * jj + 1] = with_sign_of(v[2 * jj + 1], hi);
         } else {
-          v[h] = __fdiv_rn(x, d);
+          v[2 * jj] = __fdiv_rn(lo, d);
+          v[2 * jj + 1] = __fdiv_rn(hi, d);
         }
       }
-      uint32_t b = e2m1x2_encode(v[0], v[1]);
-      packed[j >> 2] |= b << ((j & 3) * 8);
+      packed[h] = e2m1x8_encode(v);
     }
   }
   packed_out = make_uint2(packed[0], packed[1]);
@@ -154,6 +199,7 @@ __global__ void __launch_bounds__(512) k_quantize(const uint16_t* __restrict__ x
   const int64_t kc4 = K / 64;
   const int64_t col4_0 = static_cast<int64_t>(blockIdx.x) * kQuantTiles;
   const float g = __ldg(gptr);
+  const float g_inv = __frcp_rn(g);
   uint4 v[kQuantTiles][2];
 #pragma unroll
   for (int t = 0; t < kQuantTiles; ++t) {
@@ -170,7 +216,7 @@ __global__ void __launch_bounds__(512) k_quantize(const uint16_t* __restrict__ x
       const uint32_t w[8] = {v[t][0].x, v[t][0].y, v[t][0].z, v[t][0].w,
                              v[t][1].x, v[t][1].y, v[t][1].z, v[t][1].w};
       uint2 packed;
-      quantize_block(w, g, s, packed);
+      quantize_block(w, g, g_inv, s, packed);
       *reinterpret_cast<uint2*>(q + row * (K / 2) + ((col4_0 + t) * 4 + c_local) * 8) = packed;
     }
     // scale byte (r, c) of a tile sits at (r % 32) * 16 + (r / 32) * 4 + c
