@@ -541,7 +541,8 @@ def run_decode(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
 
 def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
     import torch
-    # MoE grouped: 256 experts, 512 tokens top-8 (~16 rows/expert), K = 6144, N = 4096
+    # MoE grouped: 256 experts, 512 tokens top-8 (~16 rows/expert), K = 6144, N = 4096;
+    # the same weights then routed with Zipf(1) expert popularity (skewed variant)
     E, N, K = 256, 4096, 6144
     a_rows, off, tok = synth.moe_tokens(512, E, 8, K, 3)
     Mt = int(off[-1])
@@ -566,6 +567,17 @@ def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
     gbs = mbytes / (ms * 1e-3) / 1e9
     out["moe_grouped"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
                           "bytes": mbytes, "tflops": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12}
+    a_s, off_s, _ = synth.moe_tokens(512, E, 8, K, 3, zipf_s=1.0)
+    qs, sfs, gs = quantize_dev(to_dev(a_s))
+    off_sd = to_dev(off_s)
+    ms = time_graph(lambda i: m.nvfp4_grouped_gemm(qs, sfs, gs, qb, sfb, gb, off_sd, E, Mt, N, K,
+                                                   y=y, workspace=wsp), 4, 5, stream)
+    hit = int((np.diff(off_s) > 0).sum())
+    mbytes = hit * (N * K // 2 + sfb_bytes)
+    gbs = mbytes / (ms * 1e-3) / 1e9
+    out["moe_grouped_skewed"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
+                                 "max_rows_per_expert": int(np.diff(off_s).max()), "routing": "Zipf(1) popularity",
+                                 "bytes": mbytes, "tflops": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12}
     del qb, sfb, wsp
     torch.cuda.empty_cache()
 

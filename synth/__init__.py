@@ -107,8 +107,14 @@ def normal_bf16(shape, seed: int, std: float = 1.0, outlier_p: float = 0.0,
     return out.reshape(shape)
 
 
-def route_topk(n_tokens: int, n_experts: int, topk: int, seed: int):
-    """Each token picks `topk` distinct experts uniformly (partial Fisher-Yates).
+def route_topk(n_tokens: int, n_experts: int, topk: int, seed: int, zipf_s: float = 0.0):
+    """Each token picks `topk` distinct experts.
+
+    zipf_s == 0: uniformly (partial Fisher-Yates on the token's draws).
+    zipf_s > 0: skewed; expert e has popularity (e + 1) ** -zipf_s and the token draws
+    without replacement in proportion to the popularity of the experts it has not
+    picked yet (one uniform draw per pick, inverse CDF over the remaining experts in
+    index order).
 
     Returns (token_of_row, expert_of_row, expert_offsets): the routed rows sorted
     by expert (ties by token), and offsets[E+1] with rows offsets[e]..offsets[e+1]
@@ -116,12 +122,25 @@ def route_topk(n_tokens: int, n_experts: int, topk: int, seed: int):
     """
     u = uniform01(seed, 0, n_tokens * topk).reshape(n_tokens, topk)
     choice = np.empty((n_tokens, topk), dtype=np.int64)
-    for t in range(n_tokens):
-        perm = np.arange(n_experts)
-        for j in range(topk):
-            r = j + min(int(u[t, j] * (n_experts - j)), n_experts - j - 1)
-            perm[j], perm[r] = perm[r], perm[j]
-        choice[t] = perm[:topk]
+    if zipf_s == 0.0:
+        for t in range(n_tokens):
+            perm = np.arange(n_experts)
+            for j in range(topk):
+                r = j + min(int(u[t, j] * (n_experts - j)), n_experts - j - 1)
+                perm[j], perm[r] = perm[r], perm[j]
+            choice[t] = perm[:topk]
+    else:
+        pop = (np.arange(n_experts, dtype=np.float64) + 1.0) ** (-zipf_s)
+        for t in range(n_tokens):
+            w = pop.copy()
+            for j in range(topk):
+                cdf = np.cumsum(w)
+                e = int(np.searchsorted(cdf, u[t, j] * cdf[-1], side="right"))
+                e = min(e, n_experts - 1)
+                while w[e] == 0.0:  # a draw at a removed expert's edge: next remaining one
+                    e -= 1
+                choice[t, j] = e
+                w[e] = 0.0
     tok = np.repeat(np.arange(n_tokens), topk)
     exp = choice.reshape(-1)
     order = np.lexsort((tok, exp))
@@ -149,12 +168,12 @@ def dense_inputs(M: int, N: int, K: int, seed: int, x_std=1.0, x_outlier=0.0, w_
     return x, w
 
 
-def moe_tokens(tokens: int, experts: int, topk: int, K: int, seed: int, x_std=1.0):
+def moe_tokens(tokens: int, experts: int, topk: int, K: int, seed: int, x_std=1.0, zipf_s=0.0):
     """Routed token activations, gathered into expert-sorted rows.
 
     Returns (a_rows [tokens*topk, K] bf16 bits, offsets[E+1], token_of_row).
     """
-    tok, _, offsets = route_topk(tokens, experts, topk, 1000 + seed)
+    tok, _, offsets = route_topk(tokens, experts, topk, 1000 + seed, zipf_s)
     x = normal_bf16((tokens, K), 2 * seed, x_std)
     return x[tok], offsets, tok
 

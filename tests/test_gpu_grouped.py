@@ -94,6 +94,23 @@ def test_grouped_moe_workload_sampled():
     g.check(y, rows=rows, cols=cols)
 
 
+def test_grouped_moe_skewed_routing_sampled():
+    # Zipf(1) expert popularity: expert 0 takes ~400 of the 4096 rows (7 token tiles),
+    # the tail experts one or two rows; K = 6144, N = 4096 as in the MoE workload
+    a_rows, off, tok = synth.moe_tokens(512, 256, 8, 6144, 3, zipf_s=1.0)
+    counts = np.diff(off)
+    assert counts.max() > 300
+    g = Grouped(tuple(counts), 4096, 6144, 3, a_rows=a_rows,
+                w=lambda e: synth.moe_expert_weight(e, 4096, 6144, 3))
+    y = g.run()
+    rng = np.random.default_rng(2)
+    heavy = np.arange(off[0], off[1])  # every 64-row token tile of the heaviest expert
+    rows = np.concatenate([heavy[[0, 63, 64, 127, 128, len(heavy) - 1]], [g.Mt - 1],
+                           rng.choice(g.Mt, 24, replace=False)])
+    cols = np.concatenate([[0, 127, 128, 4095], rng.choice(4096, 44, replace=False)])
+    g.check(y, rows=rows, cols=cols)
+
+
 def test_grouped_bad_offsets_reported_and_output_untouched():
     g = Grouped((4, 4, 4), 128, 256, 24)
     bad = g.off.copy()

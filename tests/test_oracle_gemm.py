@@ -204,3 +204,31 @@ def test_synth_generator_is_seeded_and_shaped():
     assert off[-1] == 4096 and (np.diff(off) >= 0).all()
     for t in range(512):
         assert len(set(exp[tok == t])) == 8
+
+
+def test_skewed_routing_is_seeded_distinct_and_zipf_ordered():
+    tok, exp, off = synth.route_topk(512, 256, 8, 1003, 1.0)
+    tok2, exp2, off2 = synth.route_topk(512, 256, 8, 1003, 1.0)
+    assert np.array_equal(exp, exp2) and np.array_equal(off, off2)
+    assert off[-1] == 4096 and (np.diff(off) >= 0).all()
+    for t in range(512):
+        assert len(set(exp[tok == t])) == 8
+    c = np.diff(off)
+    # popularity (e + 1)^-1: expert 0 is picked by most tokens, counts fall with the index
+    assert c[0] > 0.6 * 512 and c[0] > c[1] > c[4] > c[32] and c[:8].sum() > c[128:].sum()
+    # a token's first pick follows the popularity law: P(e) = (1/(e+1)) / H_256
+    first = np.array([exp[tok == t].min() for t in range(512)])
+    assert (first == 0).mean() > 0.3
+    # uniform routing is the zipf_s = 0 case, unchanged
+    tu, eu, ou = synth.route_topk(512, 256, 8, 1003)
+    tz, ez, oz = synth.route_topk(512, 256, 8, 1003, 0.0)
+    assert np.array_equal(eu, ez) and np.diff(ou).max() < 40
+
+
+def test_skewed_routing_single_draw_law():
+    # topk = 1: each token's expert is the inverse CDF of its draw over (e + 1)^-s
+    tok, exp, off = synth.route_topk(20000, 16, 1, 77, 2.0)
+    pop = (np.arange(16) + 1.0) ** -2.0
+    expect = pop / pop.sum() * 20000
+    got = np.diff(off)
+    assert np.all(np.abs(got - expect) < 5 * np.sqrt(expect) + 2)
