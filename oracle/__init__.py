@@ -242,6 +242,48 @@ def grouped_gemm(a, sfa, ga, b, sfb, gb, offsets, E, M_total, N, K, rows=None, c
     return y, ad
 
 
+def silu(v: np.ndarray) -> np.ndarray:
+    """SiLU (swish with beta = 1), float64: v * sigmoid(v) = v / (1 + exp(-v))."""
+    v = np.asarray(v, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return v / (1.0 + np.exp(-v))
+
+
+def grouped_gemm_swiglu(a, sfa, ga, b_gu, sfb_gu, gb, offsets, E, M_total, N_gu, K, rows=None, cols=None):
+    """MoE gate/up projection with the SwiGLU product fused after it.
+
+    Each expert's weight b_gu[e] holds 2I = N_gu rows interleaved row by row: row 2c is
+    gate row c, row 2c + 1 is up row c (a layout convention of the library; the pages
+    name the fused gate+up projection, "The Moment of Synthesis", Reasoning, but give no
+    layout). gate and up are the grouped GEMM's float64 outputs for those rows and
+    y[t, c] = silu(gate[t, c]) * up[t, c], c in [0, I). `cols` selects output columns c.
+    Returns (y, gate, up, absdot_gate, absdot_up).
+    """
+    I = N_gu // 2
+    c = np.arange(I) if cols is None else np.asarray(cols, dtype=np.int64)
+    gate, ad_g = grouped_gemm(a, sfa, ga, b_gu, sfb_gu, gb, offsets, E, M_total, N_gu, K, rows=rows, cols=2 * c)
+    up, ad_u = grouped_gemm(a, sfa, ga, b_gu, sfb_gu, gb, offsets, E, M_total, N_gu, K, rows=rows, cols=2 * c + 1)
+    return silu(gate) * up, gate, up, ad_g, ad_u
+
+
+def within_tolerance_swiglu(y_gpu, gate, up, ad_g, ad_u, rel: float = 4e-3, absk: float = 1e-5):
+    """Tolerance of the fused output, propagated from the GEMM tolerance of each factor.
+
+    With tg, tu the GEMM bounds (rel*|v| + absk*sum_k|x^ w^|) of gate and up, and
+    |silu'| <= 1.1 everywhere: |silu(g')u' - silu(g)u| <= 1.1 tg (|u| + tu) + |silu(g)| tu;
+    the bf16 rounding of the result adds at most 2^-8 |y|. Returns (ok, worst ratio).
+    """
+    y_ref = silu(gate) * up
+    tg = rel * np.abs(gate) + absk * ad_g
+    tu = rel * np.abs(up) + absk * ad_u
+    bound = 1.1 * tg * (np.abs(up) + tu) + np.abs(silu(gate)) * tu + 2.0 ** -8 * np.abs(y_ref)
+    err = np.abs(np.asarray(y_gpu, dtype=np.float64) - y_ref)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(bound > 0, err / bound, np.where(err > 0, np.inf, 0.0))
+    worst = float(np.max(ratio)) if ratio.size else 0.0
+    return bool(np.all(err <= bound)), worst
+
+
 def within_tolerance(y_gpu: np.ndarray, y_ref: np.ndarray, absdot: np.ndarray,
                      rel: float = 4e-3, absk: float = 1e-5):
     """Per-element |y_gpu - y_ref| <= rel*|y_ref| + absk*sum_k|x^ w^|; returns (ok, worst ratio)."""

@@ -232,3 +232,51 @@ def test_skewed_routing_single_draw_law():
     expect = pop / pop.sum() * 20000
     got = np.diff(off)
     assert np.all(np.abs(got - expect) < 5 * np.sqrt(expect) + 2)
+
+
+def test_silu_against_library_and_identities():
+    special = pytest.importorskip("scipy.special")
+    v = np.concatenate([np.linspace(-40, 40, 4001), [0.0, 1e-300, -1e-300, 700.0, -700.0]])
+    s = oracle.silu(v)
+    assert np.allclose(s, v * special.expit(v), rtol=1e-15, atol=1e-300)
+    assert oracle.silu(np.array([0.0]))[0] == 0.0
+    assert np.allclose(oracle.silu(v) - oracle.silu(-v), v, rtol=1e-14, atol=1e-14)  # silu(v) - silu(-v) = v
+
+
+def test_swiglu_oracle_is_interleaved_grouped_gemm_then_silu_times_up():
+    special = pytest.importorskip("scipy.special")
+    E, N_gu, K = 3, 48, 128
+    counts = np.array([5, 0, 7])
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    Mt = int(off[-1])
+    qa, sfa, ga = oracle.quantize(synth.normal_bf16((Mt, K), 41, 1.0))
+    sfb_bytes = oracle.scale_bytes(N_gu, K)
+    qb = np.empty((E, N_gu, K // 2), dtype=np.uint8)
+    sfb = np.empty((E, sfb_bytes), dtype=np.uint8)
+    gb = np.empty(E, dtype=np.float32)
+    for e in range(E):
+        qb[e], sfb[e], gb[e] = oracle.quantize(synth.normal_bf16((N_gu, K), 42 + e, 0.5))
+    full, _ = oracle.grouped_gemm(qa, sfa, ga, qb, sfb, gb, off, E, Mt, N_gu, K)
+    y, gate, up, adg, adu = oracle.grouped_gemm_swiglu(qa, sfa, ga, qb, sfb, gb, off, E, Mt, N_gu, K)
+    assert np.array_equal(gate, full[:, 0::2]) and np.array_equal(up, full[:, 1::2])
+    assert np.allclose(y, gate * special.expit(gate) * up, rtol=1e-14, atol=1e-300)
+    # the gate is the even row: swapping the roles gives a different product here
+    assert not np.allclose(y, up * special.expit(up) * gate)
+    cols = np.array([0, 7, 23])
+    ys, gs, us, _, _ = oracle.grouped_gemm_swiglu(qa, sfa, ga, qb, sfb, gb, off, E, Mt, N_gu, K, cols=cols)
+    assert np.array_equal(ys, y[:, cols])
+
+
+def test_swiglu_tolerance_bound_edges():
+    gate = np.array([2.0, -3.0, 0.0, 10.0])
+    up = np.array([1.5, 0.25, 4.0, -2.0])
+    adg = np.array([50.0, 10.0, 100.0, 5.0])
+    adu = np.array([20.0, 30.0, 1.0, 7.0])
+    y = oracle.silu(gate) * up
+    tg = 4e-3 * np.abs(gate) + 1e-5 * adg
+    tu = 4e-3 * np.abs(up) + 1e-5 * adu
+    bound = 1.1 * tg * (np.abs(up) + tu) + np.abs(oracle.silu(gate)) * tu + 2.0 ** -8 * np.abs(y)
+    ok, worst = oracle.within_tolerance_swiglu(y + 0.999 * bound, gate, up, adg, adu)
+    assert ok and worst < 1.0
+    ok, worst = oracle.within_tolerance_swiglu(y - 1.001 * bound, gate, up, adg, adu)
+    assert not ok and worst > 1.0
