@@ -567,6 +567,15 @@ def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
     gbs = mbytes / (ms * 1e-3) / 1e9
     out["moe_grouped"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
                           "bytes": mbytes, "tflops": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12}
+    # the same weights read as interleaved gate/up rows, SwiGLU fused into the epilogue
+    y_act = torch.empty((Mt, N // 2), dtype=torch.bfloat16, device=dev)
+    ms = time_graph(lambda i: m.nvfp4_grouped_gemm_swiglu(qa, sfa, ga, qb, sfb, gb, off_d, E, Mt, N, K,
+                                                          y=y_act, workspace=wsp), 4, 5, stream)
+    gbs = mbytes / (ms * 1e-3) / 1e9
+    out["moe_gate_up_swiglu"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
+                                 "bytes": mbytes, "out": f"bf16 [{Mt}, {N // 2}] = silu(gate) * up",
+                                 "tflops": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12}
+    del y_act
     a_s, off_s, _ = synth.moe_tokens(512, E, 8, K, 3, zipf_s=1.0)
     qs, sfs, gs = quantize_dev(to_dev(a_s))
     off_sd = to_dev(off_s)

@@ -130,6 +130,27 @@ int nvfp4_grouped_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, co
                        size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * MoE gate/up projection with the SwiGLU activation fused into the epilogue:
+ * y[m, c] = silu(gate[m, c]) * up[m, c], silu(v) = v / (1 + exp(-v)), where gate and
+ * up are the grouped GEMM's outputs for expert e's weight rows 2c and 2c + 1
+ * ("The Moment of Synthesis", magik.net, Reasoning: the per-expert N = 2048 x 2 fused
+ * gate+up projection feeding a K = 2048 down projection). Arguments as
+ * nvfp4_grouped_gemm with:
+ *   b_gu, sfb_gu     packed [E, N_gu, K/2] with gate and up rows interleaved row by row
+ *                    (row 2c gate row c, row 2c + 1 up row c; quantise the interleaved
+ *                    matrix), scales of that matrix; N_gu = 2 I, a multiple of 8
+ *   y                bf16 [M_total, N_gu / 2], written
+ *   workspace        nvfp4_grouped_gemm_workspace_bytes(E, M_total, N_gu, K) bytes
+ * The activation runs in fp32 on g_a * g_b * accumulator values before the one bf16
+ * rounding of the product; the result agrees with the oracle within the bound the
+ * GEMM tolerance of each factor implies (1.1 t_g (|u| + t_u) + |silu(g)| t_u + 2^-8 |y|).
+ */
+int nvfp4_grouped_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b_gu,
+                              const uint8_t* sfb_gu, const float* gb, const int32_t* expert_offsets, int32_t E,
+                              int64_t M_total, int64_t N_gu, int64_t K, uint16_t* y, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
  * Allocation-free variant of nvfp4_grouped_gemm. The pages have no counterpart;
  * it exists for callers that cannot call cudaMalloc at the point where they run
  * the MoE layer: code that runs while a stream is being captured into a CUDA

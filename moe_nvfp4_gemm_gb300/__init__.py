@@ -33,7 +33,8 @@ STATUS = {0: "NVFP4_OK", -1: "NVFP4_ERR_INVALID_ARG", -2: "NVFP4_ERR_UNSUPPORTED
 
 EXPORTS = ["nvfp4_status_string", "nvfp4_scale_bytes", "nvfp4_amax_workspace_bytes", "nvfp4_amax",
            "nvfp4_quantize", "nvfp4_gemm_workspace_bytes", "nvfp4_gemm",
-           "nvfp4_grouped_gemm_workspace_bytes", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_noalloc",
+           "nvfp4_grouped_gemm_workspace_bytes", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_swiglu",
+           "nvfp4_grouped_gemm_noalloc",
            "nvfp4_encode_e2m1",
            "nvfp4_encode_e4m3", "nvfp4_tune", "nvfp4_last_launch_count"]
 
@@ -78,6 +79,8 @@ def lib():
             L.nvfp4_grouped_gemm_workspace_bytes.argtypes = [_i32, _i64, _i64, _i64]
             L.nvfp4_grouped_gemm.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64,
                                              _i64, _vp, _vp, _sz, _vp, _vp]
+            L.nvfp4_grouped_gemm_swiglu.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64,
+                                                    _i64, _vp, _vp, _sz, _vp, _vp]
             L.nvfp4_grouped_gemm_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64,
                                                      _i64, _i64, _vp, _vp, _vp]
             L.nvfp4_encode_e2m1.argtypes = [_vp, _i64, _vp, _vp]
@@ -196,6 +199,27 @@ def nvfp4_grouped_gemm(a, sfa, ga, b, sfb, gb, expert_offsets, E: int, M_total: 
                                     _ptr(expert_offsets), E, M_total, N, K, _ptr(y),
                                     _ptr(workspace), workspace.numel(), _ptr(dev_status),
                                     _stream(stream)))
+    return y
+
+
+def nvfp4_grouped_gemm_swiglu(a, sfa, ga, b_gu, sfb_gu, gb, expert_offsets, E: int, M_total: int, N_gu: int,
+                              K: int, y=None, workspace=None, dev_status=None, stream=None):
+    """Gate/up projection with fused SwiGLU: b_gu interleaves gate and up rows (row 2c gate c,
+    2c + 1 up c); returns y[m, c] = silu(gate) * up as bf16 [M_total, N_gu // 2]."""
+    for t, n in ((a, "a"), (sfa, "sfa"), (b_gu, "b_gu"), (sfb_gu, "sfb_gu")):
+        _cuda(t, torch.uint8, n)
+    _cuda(ga, torch.float32, "ga")
+    _cuda(gb, torch.float32, "gb")
+    _cuda(expert_offsets, torch.int32, "expert_offsets")
+    y = torch.empty((M_total, N_gu // 2), dtype=torch.bfloat16, device=a.device) if y is None else y
+    ws_bytes = nvfp4_grouped_gemm_workspace_bytes(E, M_total, N_gu, K)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=a.device)
+    _check("nvfp4_grouped_gemm_swiglu",
+           lib().nvfp4_grouped_gemm_swiglu(_ptr(a), _ptr(sfa), _ptr(ga), _ptr(b_gu), _ptr(sfb_gu), _ptr(gb),
+                                           _ptr(expert_offsets), E, M_total, N_gu, K, _ptr(y),
+                                           _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                                           _stream(stream)))
     return y
 
 

@@ -393,10 +393,10 @@ size_t nvfp4_grouped_gemm_workspace_bytes(int32_t E, int64_t M_total, int64_t N,
   return static_cast<size_t>(grouped_slab_offset(E, M_total) + grouped_max_tiles(E, M_total) * (K / 64) * 512);
 }
 
-int nvfp4_grouped_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b, const uint8_t* sfb,
-                       const float* gb, const int32_t* expert_offsets, int32_t E, int64_t M_total, int64_t N,
-                       int64_t K, uint16_t* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                       void* stream) {
+static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b, const uint8_t* sfb,
+                        const float* gb, const int32_t* expert_offsets, int32_t E, int64_t M_total, int64_t N,
+                        int64_t K, uint16_t* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        void* stream, int swiglu) {
   g_last_launches = 0;
   if (E <= 0) return NVFP4_ERR_INVALID_ARG;
   int rc = check_gemm_shape(M_total, N, K);
@@ -448,6 +448,7 @@ int nvfp4_grouped_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, co
   s.x_rows = kGroupTileRows;
   s.acc_cols = kGroupTileRows;
   s.acc_bufs = 2;
+  s.swiglu = swiglu;
   const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0) - 1536;
   int stages = g_tune.grouped_stages;
   if (stages == 0) stages = (kSmemLimit - 1536) / stage_bytes;
@@ -461,6 +462,22 @@ int nvfp4_grouped_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, co
   rc = from_cuda(launch_stream(tmW, tmX, s, true, grid, st));
   g_last_launches = 2;
   return rc;
+}
+
+int nvfp4_grouped_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b, const uint8_t* sfb,
+                       const float* gb, const int32_t* expert_offsets, int32_t E, int64_t M_total, int64_t N,
+                       int64_t K, uint16_t* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                       void* stream) {
+  return grouped_impl(a, sfa, ga, b, sfb, gb, expert_offsets, E, M_total, N, K, y, workspace, workspace_bytes,
+                      dev_status, stream, 0);
+}
+
+int nvfp4_grouped_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b_gu,
+                              const uint8_t* sfb_gu, const float* gb, const int32_t* expert_offsets, int32_t E,
+                              int64_t M_total, int64_t N_gu, int64_t K, uint16_t* y, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return grouped_impl(a, sfa, ga, b_gu, sfb_gu, gb, expert_offsets, E, M_total, N_gu, K, y, workspace,
+                      workspace_bytes, dev_status, stream, 1);
 }
 
 }  // extern "C"

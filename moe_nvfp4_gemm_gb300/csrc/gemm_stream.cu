@@ -411,7 +411,22 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         __syncwarp();
         if (elect_one()) mbar_arrive(&tempty[buf]);
         __syncwarp();
-        if (wrow < N) {
+        if (p.swiglu) {
+          // Weight rows 2c and 2c + 1 (gate and up of output column c) sit in adjacent
+          // lanes: the even lane takes its partner's value and writes silu(gate) * up.
+          const int n_out = N >> 1;
+#pragma unroll
+          for (int j = 0; j < MAXC; ++j)
+            if (j < it.rows) {
+              const float v = __uint_as_float(r[j]) * alpha;
+              const float up = __shfl_xor_sync(0xffffffffu, v, 1);
+              if ((lane & 1) == 0 && wrow < N) {
+                const float act = v / (1.0f + __expf(-v));
+                p.y[static_cast<int64_t>(it.row0 + j) * n_out + (wrow >> 1)] =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(act * up));
+              }
+            }
+        } else if (wrow < N) {
 #pragma unroll
           for (int j = 0; j < MAXC; ++j)
             if (j < it.rows)

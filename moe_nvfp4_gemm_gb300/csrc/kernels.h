@@ -36,6 +36,7 @@ struct StreamArgs {
   int acc_bufs;
   int tmem_cols;
   int pdl;                 // launched with programmatic stream serialization
+  int swiglu;              // grouped: weight rows interleave gate/up; y[t, c] = silu(gate) * up, N / 2 wide
 };
 
 

@@ -45,6 +45,25 @@ class Grouped:
         torch.cuda.synchronize()
         return y
 
+    def run_swiglu(self):
+        y = m.nvfp4_grouped_gemm_swiglu(to_dev(self.qa), to_dev(self.sfa), scalar(self.ga), to_dev(self.qb),
+                                        to_dev(self.sfb), to_dev(self.gb), to_dev(self.off), self.E, self.Mt,
+                                        self.N, self.K)
+        torch.cuda.synchronize()
+        return y
+
+    def check_swiglu(self, y, rows=None, cols=None):
+        yr, gate, up, adg, adu = oracle.grouped_gemm_swiglu(self.qa, self.sfa, self.ga, self.qb, self.sfb,
+                                                            self.gb, self.off, self.E, self.Mt, self.N, self.K,
+                                                            rows=rows, cols=cols)
+        yg = y.float().cpu().numpy()
+        if rows is not None:
+            yg = yg[np.asarray(rows)]
+        if cols is not None:
+            yg = yg[:, np.asarray(cols)]
+        ok, worst = oracle.within_tolerance_swiglu(yg, gate, up, adg, adu)
+        assert ok, f"swiglu parity failed: worst ratio {worst}"
+
     def check(self, y, rows=None, cols=None):
         yr, ad = oracle.grouped_gemm(self.qa, self.sfa, self.ga, self.qb, self.sfb, self.gb, self.off,
                                      self.E, self.Mt, self.N, self.K, rows=rows, cols=cols)
@@ -129,3 +148,41 @@ def test_grouped_bad_offsets_reported_and_output_untouched():
                          to_dev(g.gb), to_dev(bad), g.E, g.Mt, g.N, g.K, y=y, dev_status=st)
     torch.cuda.synchronize()
     assert st.item() == -8
+
+
+@pytest.mark.parametrize("counts,N_gu,K", [
+    ((3, 0, 17, 1, 0, 9), 256, 512),           # ragged, empty experts
+    ((64, 65, 1, 127, 0), 136, 1088),          # tile-boundary counts, N_gu not a multiple of 128
+    ((0, 200, 0), 512, 256),                   # one expert, several token tiles
+])
+def test_grouped_swiglu_matches_oracle(counts, N_gu, K):
+    g = Grouped(counts, N_gu, K, 31)
+    y = g.run_swiglu()
+    assert tuple(y.shape) == (g.Mt, N_gu // 2)
+    g.check_swiglu(y)
+
+
+def test_grouped_swiglu_is_silu_of_even_rows_times_odd_rows_of_the_plain_gemm():
+    # the fused epilogue against the unfused grouped GEMM's own output (same kernel path,
+    # same accumulators): silu(y[:, 0::2]) * y[:, 1::2] up to the bf16 rounding of y
+    g = Grouped((12, 40, 0, 70), 384, 768, 32)
+    y_plain = g.run().float()
+    y_fused = g.run_swiglu().float()
+    gate, up = y_plain[:, 0::2].double(), y_plain[:, 1::2].double()
+    ref = gate / (1 + torch.exp(-gate)) * up
+    err = (y_fused.double() - ref).abs()
+    assert (err <= 2 ** -6 * ref.abs() + 1e-3 * ref.abs().max()).all()
+
+
+def test_grouped_swiglu_moe_workload_sampled():
+    # gate+up of the MoE workload: 256 experts, 512 tokens top-8, K = 6144, N_gu = 4096 (I = 2048)
+    a_rows, off, tok = synth.moe_tokens(512, 256, 8, 6144, 3)
+    counts = np.diff(off)
+    g = Grouped(tuple(counts), 4096, 6144, 3, a_rows=a_rows,
+                w=lambda e: synth.moe_expert_weight(e, 4096, 6144, 3))
+    y = g.run_swiglu()
+    rng = np.random.default_rng(3)
+    rows = np.concatenate([[0, g.Mt - 1], rng.choice(g.Mt, 30, replace=False)])
+    cols = np.concatenate([[0, 63, 64, 2047], rng.choice(2048, 40, replace=False)])
+    g.check_swiglu(y, rows=rows, cols=cols)
+
