@@ -616,6 +616,19 @@ def run_prefill(m, synth, dev, stream, to_dev, quantize_dev, hbm, fp4_peak, out)
         m.nvfp4_gemm(q, sf, g, wcopies[i % 2][0], wcopies[i % 2][1], gw, Mp, Np, Kp, y=yp)
 
     ms_t = time_launches(together, 20, stream)
+    # layer chain: the GEMM's output as the next layer's NVFP4 input, with a given global
+    # scale: quantised in the GEMM epilogue vs bf16 out + a separate quantize pass
+    g_y = torch.full((1,), 2.0 ** -6, dtype=torch.float32, device=dev)
+    qy = torch.empty((Mp, Np // 2), dtype=torch.uint8, device=dev)
+    sfy = torch.empty(m.nvfp4_scale_bytes(Mp, Np), dtype=torch.uint8, device=dev)
+    ms_gq = time_launches(lambda i: m.nvfp4_gemm_quantize_out(q, sf, g, wcopies[i % 2][0], wcopies[i % 2][1], gw,
+                                                              g_y, Mp, Np, Kp, q_out=qy, sf_out=sfy), 20, stream)
+
+    def gemm_then_quantize(i):
+        m.nvfp4_gemm(q, sf, g, wcopies[i % 2][0], wcopies[i % 2][1], gw, Mp, Np, Kp, y=yp)
+        m.nvfp4_quantize(yp, g_y, qy, sfy)
+
+    ms_gtq = time_launches(gemm_then_quantize, 20, stream)
     qbytes = Mp * Kp * 2 + Mp * Kp // 2 + m.nvfp4_scale_bytes(Mp, Kp)
     out["prefill"] = {
         "quantize_us": ms_q * 1e3, "quantize_GBps": qbytes / (ms_q * 1e-3) / 1e9,
@@ -623,7 +636,9 @@ def run_prefill(m, synth, dev, stream, to_dev, quantize_dev, hbm, fp4_peak, out)
         "amax_us": ms_amax * 1e3, "amax_GBps": Mp * Kp * 2 / (ms_amax * 1e-3) / 1e9,
         "gemm_us": ms_g * 1e3, "gemm_tflops": 2.0 * Mp * Np * Kp / (ms_g * 1e-3) / 1e12,
         "gemm_frac": 2.0 * Mp * Np * Kp / (ms_g * 1e-3) / 1e12 / fp4_peak,
-        "together_us": ms_t * 1e3}
+        "together_us": ms_t * 1e3,
+        "gemm_nvfp4_out_us": ms_gq * 1e3, "gemm_nvfp4_out_tflops": 2.0 * Mp * Np * Kp / (ms_gq * 1e-3) / 1e12,
+        "gemm_then_quantize_us": ms_gtq * 1e3}
 
 
 if __name__ == "__main__":

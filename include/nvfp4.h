@@ -107,6 +107,24 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
                size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * NVFP4 GEMM whose epilogue emits NVFP4 instead of bf16: y = bf16(x^ . W^T^ * g_a * g_b)
+ * as in nvfp4_gemm, then each 16-column block of y quantised with the caller's global
+ * scale by the nvfp4_quantize recipe (the quantisation-overhead remark of "Blackwell
+ * NVFP4 GEMM", What is this?: a layer chain otherwise re-reads y to quantise it).
+ *   g_out    device fp32, decode-direction global scale of the output (for example from
+ *            calibration, or nvfp4_amax of an earlier batch); blocks whose values exceed
+ *            the range it allows saturate, as in nvfp4_quantize
+ *   q_out    [M, N/2] packed E2M1 codes, written
+ *   sf_out   nvfp4_scale_bytes(M, N) bytes in the 128 x 4 tiled layout, written
+ *            (padding rows up to a multiple of 128 written as zero)
+ * N must be a multiple of 64. Codes and scales equal nvfp4_quantize applied to the bf16
+ * values nvfp4_gemm returns for the same operands (bit for bit).
+ */
+int nvfp4_gemm_quantize_out(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b,
+                            const uint8_t* sfb, const float* gb, const float* g_out, uint8_t* q_out, uint8_t* sf_out,
+                            int64_t M, int64_t N, int64_t K, int32_t* dev_status, void* stream);
+
+/*
  * Grouped (MoE) NVFP4 GEMM: for each expert e and each row m with
  * expert_offsets[e] <= m < expert_offsets[e+1], y[m, :] = x[m, :] @ W_e^T
  * ("The Moment of Synthesis", magik.net, Reasoning: grouped GEMM over the

@@ -32,7 +32,7 @@ STATUS = {0: "NVFP4_OK", -1: "NVFP4_ERR_INVALID_ARG", -2: "NVFP4_ERR_UNSUPPORTED
           -6: "NVFP4_ERR_WORKSPACE", -7: "NVFP4_ERR_TIMEOUT", -8: "NVFP4_ERR_BAD_OFFSETS"}
 
 EXPORTS = ["nvfp4_status_string", "nvfp4_scale_bytes", "nvfp4_amax_workspace_bytes", "nvfp4_amax",
-           "nvfp4_quantize", "nvfp4_gemm_workspace_bytes", "nvfp4_gemm",
+           "nvfp4_quantize", "nvfp4_gemm_workspace_bytes", "nvfp4_gemm", "nvfp4_gemm_quantize_out",
            "nvfp4_grouped_gemm_workspace_bytes", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_swiglu",
            "nvfp4_grouped_gemm_noalloc",
            "nvfp4_encode_e2m1",
@@ -75,6 +75,8 @@ def lib():
             L.nvfp4_gemm_workspace_bytes.argtypes = [_i64, _i64, _i64]
             L.nvfp4_gemm.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz,
                                      _vp, _vp]
+            L.nvfp4_gemm_quantize_out.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                                  _i64, _vp, _vp]
             L.nvfp4_grouped_gemm_workspace_bytes.restype = _sz
             L.nvfp4_grouped_gemm_workspace_bytes.argtypes = [_i32, _i64, _i64, _i64]
             L.nvfp4_grouped_gemm.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64,
@@ -180,6 +182,24 @@ def nvfp4_gemm(a, sfa, ga, b, sfb, gb, M: int, N: int, K: int, y=None, dev_statu
 
 def nvfp4_grouped_gemm_workspace_bytes(E: int, M_total: int, N: int, K: int) -> int:
     return int(lib().nvfp4_grouped_gemm_workspace_bytes(E, M_total, N, K))
+
+
+def nvfp4_gemm_quantize_out(a, sfa, ga, b, sfb, gb, g_out, M: int, N: int, K: int, q_out=None, sf_out=None,
+                            dev_status=None, stream=None):
+    """y = x . W^T as nvfp4_gemm, emitted as NVFP4 with global scale g_out: returns
+    (codes uint8 [M, N/2], tiled scales uint8 [nvfp4_scale_bytes(M, N)])."""
+    for t, n in ((a, "a"), (sfa, "sfa"), (b, "b"), (sfb, "sfb")):
+        _cuda(t, torch.uint8, n)
+    for t, n in ((ga, "ga"), (gb, "gb"), (g_out, "g_out")):
+        _cuda(t, torch.float32, n)
+    if q_out is None:
+        q_out = torch.empty((M, N // 2), dtype=torch.uint8, device=a.device)
+    if sf_out is None:
+        sf_out = torch.empty(nvfp4_scale_bytes(M, N), dtype=torch.uint8, device=a.device)
+    _check("nvfp4_gemm_quantize_out",
+           lib().nvfp4_gemm_quantize_out(_ptr(a), _ptr(sfa), _ptr(ga), _ptr(b), _ptr(sfb), _ptr(gb), _ptr(g_out),
+                                         _ptr(q_out), _ptr(sf_out), M, N, K, _ptr(dev_status), _stream(stream)))
+    return q_out, sf_out
 
 
 def nvfp4_grouped_gemm(a, sfa, ga, b, sfb, gb, expert_offsets, E: int, M_total: int, N: int,

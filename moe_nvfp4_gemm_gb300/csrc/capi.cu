@@ -381,6 +381,39 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
   return rc;
 }
 
+int nvfp4_gemm_quantize_out(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b,
+                            const uint8_t* sfb, const float* gb, const float* g_out, uint8_t* q_out, uint8_t* sf_out,
+                            int64_t M, int64_t N, int64_t K, int32_t* dev_status, void* stream) {
+  g_last_launches = 0;
+  int rc = check_gemm_shape(M, N, K);
+  if (rc) return rc;
+  if (N % 64 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;  // whole 4-block scale groups per row
+  if (M == 0) return NVFP4_OK;
+  if (!a || !sfa || !ga || !b || !sfb || !gb || !g_out || !q_out || !sf_out) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(q_out) ||
+      !aligned16(sf_out))
+    return NVFP4_ERR_ALIGNMENT;
+  DevInfo d;
+  rc = device_info(d);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CUtensorMap tmA, tmB, tmSFA, tmSFB, tmY;
+  if ((rc = encode_2d(&tmA, a, M, K / 2, 128))) return rc;
+  if ((rc = encode_2d(&tmB, b, N, K / 2, 128))) return rc;
+  if ((rc = encode_sf(&tmSFA, sfa, nvfp4_scale_bytes(M, K) / 512))) return rc;
+  if ((rc = encode_sf(&tmSFB, sfb, nvfp4_scale_bytes(N, K) / 512))) return rc;
+  tmY = tmA;  // unused by the quantising epilogue
+  DenseArgs da = {sfa, sfb, ga, gb, nullptr, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                  dev_status, q_out, sf_out, g_out};
+  const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
+  int pairs = (g_tune.dense_grid ? g_tune.dense_grid : d.sms) / 2;
+  if (pairs > tiles) pairs = static_cast<int>(tiles);
+  if (pairs < 1) pairs = 1;
+  rc = from_cuda(launch_dense_pair(tmA, tmB, tmSFA, tmSFB, tmY, da, 2 * pairs, st, true));
+  g_last_launches = 1;
+  return rc;
+}
+
 static int64_t grouped_max_tiles(int32_t E, int64_t M_total) { return (M_total + kGroupTileRows - 1) / kGroupTileRows + E; }
 
 static int64_t grouped_slab_offset(int32_t E, int64_t M_total) {

@@ -25,6 +25,7 @@
 #include <stdint.h>
 
 #include "kernels.h"
+#include "nvfp4_quant.cuh"
 #include "ptx.cuh"
 
 namespace nvfp4 {
@@ -235,6 +236,9 @@ struct PairCfg {
   static_assert(STAGE_BYTES % 1024 == 0, "swizzled buffers stay 1024-byte aligned");
 };
 
+// QOUT: the epilogue quantises the bf16 results to NVFP4 (codes, tiled block scales)
+// with the caller's global scale instead of writing bf16.
+template <bool QOUT>
 __global__ void __launch_bounds__(kPairThreads, 1)
     k_gemm_dense_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -403,16 +407,75 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const float alpha = __ldg(p.ga) * __ldg(p.gb);
     uint8_t* buf = out_buf + (warp - 2) * 4096;
     const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
+    float g_q = 1.0f, g_q_inv = 1.0f;
+    if (QOUT) {
+      g_q = __ldg(p.g_out);
+      g_q_inv = __frcp_rn(g_q);
+    }
     uint32_t acc_ph = 0;
     for (int t = pair; t < tiles; t += npairs) {
       const int m_blk = t % mt, n_blk = t / mt;
       if (!mbar_wait_warp(tfull, acc_ph, abort_flag)) break;
       tc_fence_after();
-      drain_accumulator_tma<128>(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128, alpha, buf, &tmY,
-                                 n_blk * 256 + h * 128, m_blk * 256 + rank * 128 + q * 32, [&] {
-                                   if (elect_one()) mbar_arrive_cluster(tempty_leader);
-                                   __syncwarp();
-                                 });
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
+      const int row0 = m_blk * 256 + rank * 128 + q * 32;
+      const int col0 = n_blk * 256 + h * 128;
+      if (QOUT) {
+        // Each thread owns one output row's 128 columns = 8 blocks of 16: block amax,
+        // E4M3 scale and E2M1 codes are thread-local (the stand-alone quantiser's recipe
+        // on the same bf16 values the plain epilogue would store).
+        uint32_t r[128];
+#pragma unroll
+        for (int c = 0; c < 128; c += 32) tmem_ld32(taddr + c, r + c);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (elect_one()) mbar_arrive_cluster(tempty_leader);
+        __syncwarp();
+        uint32_t wb[64];  // the 128 results as bf16 pairs (the fp32 values are dead after this)
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          wb[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * alpha, __uint_as_float(r[2 * j + 1]) * alpha);
+        const int row = row0 + lane;
+        const int Nc4 = N / 64;  // 4-block scale groups per row (N % 64 == 0)
+        const int pad_rows = (M + 127) / 128 * 128;
+        if (row < pad_rows) {
+          uint32_t sw[2] = {0u, 0u};
+#pragma unroll
+          for (int bp = 0; bp < 4; ++bp) {  // pairs of blocks: 32 columns, 16 bytes of codes
+            uint2 packed[2];
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+              const int blk = bp * 2 + hb;
+              uint32_t w[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) w[j] = wb[blk * 8 + j];
+              uint32_t sc = 0;
+              packed[hb] = make_uint2(0u, 0u);
+              if (row < M) quantize_block(w, g_q, g_q_inv, sc, packed[hb]);
+              sw[blk >> 2] |= sc << ((blk & 3) * 8);
+            }
+            if (row < M && col0 + bp * 32 < N)
+              st_global_v4(p.q_out + static_cast<int64_t>(row) * (N / 2) + (col0 + bp * 32) / 2, packed[0].x,
+                           packed[0].y, packed[1].x, packed[1].y);
+          }
+          // scale bytes (row, c .. c + 3) of the 128 x 4 tile layout form one word
+#pragma unroll
+          for (int gi = 0; gi < 2; ++gi) {
+            const int cg = col0 / 64 + gi;  // 4-block group index
+            if (cg < Nc4) {
+              const int64_t off = (static_cast<int64_t>(row / 128) * Nc4 + cg) * 512 + (row % 32) * 16 +
+                                  ((row % 128) / 32) * 4;
+              *reinterpret_cast<uint32_t*>(p.sf_out + off) = sw[gi];
+            }
+          }
+        }
+      } else {
+        drain_accumulator_tma<128>(taddr, alpha, buf, &tmY, col0, row0, [&] {
+          if (elect_one()) mbar_arrive_cluster(tempty_leader);
+          __syncwarp();
+        });
+      }
       acc_ph ^= 1;
     }
     if (lane == 0) bulk_wait_group0();  // this warp's stores are complete before the CTA exits
@@ -451,8 +514,9 @@ cudaError_t launch_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const D
 // grid: an even number of CTAs (two per 256 x 256 tile in flight).
 cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
                               const CUtensorMap& tmSFB, const CUtensorMap& tmY, const DenseArgs& a, int grid,
-                              cudaStream_t st) {
-  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_gemm_dense_pair));
+                              cudaStream_t st, bool quantized_out) {
+  auto kernel = quantized_out ? k_gemm_dense_pair<true> : k_gemm_dense_pair<false>;
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(kernel));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -466,7 +530,7 @@ cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, co
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k_gemm_dense_pair, tmA, tmB, tmSFA, tmSFB, tmY, a);
+  e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmSFA, tmSFB, tmY, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

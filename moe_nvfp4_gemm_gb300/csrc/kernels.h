@@ -15,6 +15,11 @@ struct DenseArgs {
   uint16_t* y;
   int M, N, K;
   int32_t* status;
+  // NVFP4 output (k_gemm_dense_pair<true>): codes [M, N/2], tiled scales of [M, N], with
+  // the caller's global scale; y is not written
+  uint8_t* q_out;
+  uint8_t* sf_out;
+  const float* g_out;
 };
 
 struct StreamArgs {
@@ -51,7 +56,7 @@ cudaError_t launch_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const D
                          cudaStream_t st);
 cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
                               const CUtensorMap& tmSFB, const CUtensorMap& tmY, const DenseArgs& a, int grid,
-                              cudaStream_t st);
+                              cudaStream_t st, bool quantized_out = false);
 cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, bool grouped,
                           int grid, cudaStream_t st);
 cudaError_t launch_grouped_prep(const int32_t* offsets, int E, int M_total, int K, const uint8_t* sfx,

@@ -13,36 +13,10 @@
 #include <stdint.h>
 
 #include "kernels.h"
+#include "nvfp4_quant.cuh"
 #include "ptx.cuh"
 
 namespace nvfp4 {
-
-DEVI uint32_t e4m3_encode(float t) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(t));
-  return r & 0xFFu;
-}
-
-DEVI float e4m3_decode(uint32_t code) {
-  uint32_t h2;
-  uint16_t in = static_cast<uint16_t>(code & 0xFFu);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
-}
-
-// Two E2M1 codes in one byte: `lo` in bits 0-3, `hi` in bits 4-7.
-DEVI uint32_t e2m1x2_encode(float lo, float hi) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
-      "cvt.u32.u8 %0, t;\n\t}"
-      : "=r"(r)
-      : "f"(hi), "f"(lo));
-  return r;
-}
-
-DEVI float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-DEVI float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ---- amax ------------------------------------------------------------------------
 
@@ -96,94 +70,6 @@ __global__ void __launch_bounds__(256) k_amax_final(const float* __restrict__ pa
 // ---- block quantiser -----------------------------------------------------------
 
 constexpr int kQuantTiles = 4;  // 512-byte scale tiles (128 rows x 64 columns) per CTA
-
-// Packed pair of fp32 (Blackwell's f32x2 datapath: two IEEE round-to-nearest
-// operations per instruction, lane by lane).
-DEVI uint64_t f2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-DEVI void f2_split(uint64_t v, float& lo, float& hi) { asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v)); }
-DEVI uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-DEVI uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-// v with the sign bit of x: the quotient of a nonzero x already has x's sign, and a
-// zero x (either sign) must keep its own (the correction step below yields +0 for -0).
-DEVI float with_sign_of(float v, float x) {
-  return __uint_as_float((__float_as_uint(v) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
-}
-// Eight E2M1 codes, element 2j in the low nibble of byte j.
-DEVI uint32_t e2m1x8_encode(const float (&v)[8]) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
-      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
-      : "=r"(r)
-      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
-  return r;
-}
-
-// RN(x / d) given y = RN(1 / d): one Markstein correction of RN(x y), exact when x, d
-// and the quotient stay well inside the normal range; otherwise the IEEE division.
-DEVI float div_rn_by(float x, float d, float y) {
-  const float ax = fabsf(x);
-  if (ax < 1e-30f || ax > 1e30f || d < 1e-30f || d > 1e30f) return __fdiv_rn(x, d);
-  const float q0 = __fmul_rn(x, y);
-  return __fmaf_rn(__fmaf_rn(-q0, d, x), y, q0);
-}
-
-// g_inv = RN(1 / g), computed once per thread.
-DEVI void quantize_block(const uint32_t (&w)[8], float g, float g_inv, uint32_t& s, uint2& packed_out) {
-  float amax = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(w[j])), fabsf(bf16hi(w[j]))));
-  // RN(RN(amax / 6) / g); 0x3e2aaaab = RN(1 / 6)
-  const float t = amax == 0.0f ? 0.0f : div_rn_by(div_rn_by(amax, 6.0f, __uint_as_float(0x3e2aaaabu)), g, g_inv);
-  s = e4m3_encode(t);
-  uint32_t packed[2] = {0u, 0u};
-  if (s != 0) {
-    const float d = __fmul_rn(e4m3_decode(s), g);
-    // x / d correctly rounded without a division per element: y = RN(1/d), q0 = RN(x y)
-    // is within one ulp of x / d, the remainder x - q0 d is exact (fma), and
-    // RN(q0 + rem * y) = RN(x / d) by Markstein's theorem when nothing over- or
-    // underflows. Blocks outside that range take IEEE division.
-    const float y = __frcp_rn(d);
-    const bool fast = d > 1e-30f && d < 1e30f && __fmul_rn(amax, y) < 1e30f;
-    const uint64_t yy = f2(y, y), nd = f2(-d, -d);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {  // eight elements (one output word) at a time
-      float v[8];
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const float lo = bf16lo(w[h * 4 + jj]), hi = bf16hi(w[h * 4 + jj]);
-        if (fast) {
-          const uint64_t xx = f2(lo, hi);
-          const uint64_t q0 = f2_mul(xx, yy);
-          const uint64_t rem = f2_fma(q0, nd, xx);  // x - q0 d, exact
-          f2_split(f2_fma(rem, yy, q0), v[2 * jj], v[2 * jj + 1]);
-          v[2 * jj] = with_sign_of(v[2 * jj], lo);
-          v[2 * jj + 1] = with_sign_of(v[2 * jj + 1], hi);
-        } else {
-          v[2 * jj] = __fdiv_rn(lo, d);
-          v[2 * jj + 1] = __fdiv_rn(hi, d);
-        }
-      }
-      packed[h] = e2m1x8_encode(v);
-    }
-  }
-  packed_out = make_uint2(packed[0], packed[1]);
-}
 
 // One CTA = 128 rows x (64 * kQuantTiles) columns; thread i handles row i/4 and
 // 16-element block i%4 of each 64-column group. All of a thread's loads are issued
