@@ -71,6 +71,13 @@ def test_quantize_bit_exact(M, K, seed, std, out):
     _quantize_and_compare(synth.normal_bf16((M, K), seed, std, out))
 
 
+@pytest.mark.parametrize("M,K", [(1000, 64 * 37), (4096 + 7, 1024 + 64), (129, 64)])
+def test_quantize_ragged_edges_bit_exact(M, K):
+    # K not a multiple of 256 (partial last CTA column group), rows not a multiple of 128,
+    # a single 64-column group
+    _quantize_and_compare(synth.normal_bf16((M, K), 9, 0.5, 1e-3))
+
+
 def test_quantize_adversarial_blocks():
     K = 256
     rows = []
