@@ -82,18 +82,23 @@ DEVI uint32_t e2m1x8_encode(const float (&v)[8]) {
 
 // RN(x / d) given y = RN(1 / d): one Markstein correction of RN(x y), exact when x, d
 // and the quotient stay well inside the normal range; otherwise the IEEE division.
+// The fast path requires x, d and the quotient all in [1e-30, 1e30] in magnitude, so that
+// no intermediate over- or underflows (the remainder stays a normal number).
 DEVI float div_rn_by(float x, float d, float y) {
-  const float ax = fabsf(x);
-  if (ax < 1e-30f || ax > 1e30f || d < 1e-30f || d > 1e30f) return __fdiv_rn(x, d);
   const float q0 = __fmul_rn(x, y);
+  const float ax = fabsf(x), aq = fabsf(q0);
+  if (!(ax >= 1e-30f && ax <= 1e30f && aq >= 1e-30f && aq <= 1e30f && d >= 1e-30f && d <= 1e30f))
+    return __fdiv_rn(x, d);
   return __fmaf_rn(__fmaf_rn(-q0, d, x), y, q0);
 }
 
 // g_inv = RN(1 / g), computed once per thread.
 DEVI void quantize_block(const uint32_t (&w)[8], float g, float g_inv, uint32_t& s, uint2& packed_out) {
-  float amax = 0.0f;
+  // |x| of both halves at once (sign bits cleared), maximum on the bf16 pairs (exact)
+  uint32_t m2 = w[0] & 0x7FFF7FFFu;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(w[j])), fabsf(bf16hi(w[j]))));
+  for (int j = 1; j < 8; ++j) asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(w[j] & 0x7FFF7FFFu));
+  const float amax = fmaxf(bf16lo(m2), bf16hi(m2));
   // RN(RN(amax / 6) / g); 0x3e2aaaab = RN(1 / 6)
   const float t = amax == 0.0f ? 0.0f : div_rn_by(div_rn_by(amax, 6.0f, __uint_as_float(0x3e2aaaabu)), g, g_inv);
   s = e4m3_encode(t);

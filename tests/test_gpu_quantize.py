@@ -106,6 +106,14 @@ def test_quantize_prefill_size_bit_exact():
     _quantize_and_compare(xb)
 
 
+@pytest.mark.parametrize("g", [1e-30, 3e-36, 1e30, 2.5e35])
+def test_quantize_extreme_global_scales_bit_exact(g):
+    # block scales (amax / 6) / g far above 448 (saturate) or far below the smallest E4M3
+    # subnormal (all codes zero): the quotients leave the fast path's exact range
+    xb = synth.normal_bf16((256, 512), 10, 1.0, 1e-2)
+    _quantize_and_compare(xb, np.float32(g))
+
+
 def test_amax_zero_tensor_gives_unit_scale():
     x = torch.zeros(1000, dtype=torch.bfloat16, device=dev())
     amax, g = m.nvfp4_amax(x)
