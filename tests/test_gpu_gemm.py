@@ -110,6 +110,32 @@ def test_square_workload_sampled():
     assert torch.isfinite(y.float()).all()
 
 
+def test_prefill_workload_sampled():
+    # prefill GEMM in the benchmark's configuration: x 4096 x 8192 (N(0,1) + 0.1% x20, seed 8)
+    # against W 28672 x 8192 (N(0, 0.02), seed 9); 112 column tiles, 23.6 tiles per CTA pair
+    A = Operand(synth.normal_bf16((4096, 8192), 8, 1.0, 1e-3))
+    B = Operand(synth.normal_bf16((28672, 8192), 9, 0.02))
+    y = _run(A, B)
+    rng = np.random.default_rng(4)
+    rows = np.concatenate([[0, 255, 256, 4095], rng.choice(4096, 44, replace=False)])
+    cols = np.concatenate([[0, 255, 256, 28671], rng.choice(28672, 92, replace=False)])
+    check_gemm(y, A, B, rows=rows, cols=cols)
+    assert torch.isfinite(y.float()).all()
+
+
+@pytest.mark.parametrize("M,N,K,max_m", [
+    (256, 512, 65536, -1),    # CTA-pair kernel, 256 K blocks per tile
+    (32, 384, 131072, 128),   # streaming kernel, split-K clusters over 512 K blocks
+    (128, 256, 32768, 128),   # the largest M the streaming kernel takes
+])
+def test_long_k_sampled(M, N, K, max_m):
+    A, B = dense_case(M, N, K, 14, 1.0, 1e-3, 0.02)
+    m.nvfp4_tune(m.NVFP4_TUNE_STREAM_MAX_M, max_m)
+    y = _run(A, B)
+    cols = np.random.default_rng(K).choice(N, 48, replace=False)
+    check_gemm(y, A, B, cols=cols)
+
+
 def test_status_untouched_on_success():
     A, B = dense_case(64, 128, 256, 3)
     st = torch.zeros(1, dtype=torch.int32, device=dev())
