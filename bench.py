@@ -524,10 +524,12 @@ def run_decode(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
         xa, sfa, ga = quantize_dev(to_dev(x))
         y = torch.empty((M, SQ), dtype=torch.bfloat16, device=dev)
         fn = lambda i: m.nvfp4_gemm(xa, sfa, ga, copies[i % 8][0], copies[i % 8][1], gw, M, SQ, SQ, y=y)
-        ms = time_graph(fn, 16, 20, stream)
+        ms = time_graph(fn, 16, 20, stream)  # library default: set-up-only programmatic launch
         ms_eager = time_launches(fn, 100, stream)
         m.nvfp4_tune(m.NVFP4_TUNE_PDL, 1)
         ms_pdl = time_graph(fn, 16, 20, stream)
+        m.nvfp4_tune(m.NVFP4_TUNE_PDL, -1)
+        ms_plain = time_graph(fn, 16, 20, stream)
         m.nvfp4_tune(m.NVFP4_TUNE_PDL, 0)
         gbs = wbytes / (ms * 1e-3) / 1e9
         gbs_pdl = wbytes / (ms_pdl * 1e-3) / 1e9
@@ -535,7 +537,11 @@ def run_decode(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
                                "bytes": wbytes, "timing": "CUDA graph of 16 calls over 8 weight copies",
                                "us_eager_per_launch_events": ms_eager * 1e3,
                                "us_pdl": ms_pdl * 1e3, "weight_GBps_pdl": gbs_pdl,
-                               "hbm_frac_pdl": gbs_pdl / hbm}
+                               "hbm_frac_pdl": gbs_pdl / hbm,
+                               "pdl_note": "us: default (set-up overlaps the previous call, always ordered); "
+                                           "us_pdl: weights also requested before the wait (static weights); "
+                                           "us_plain_stream_order: no overlap",
+                               "us_plain_stream_order": ms_plain * 1e3}
     del copies, wq, sfw
 
 

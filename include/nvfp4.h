@@ -220,13 +220,15 @@ int nvfp4_encode_e4m3(const float* v, int64_t n, uint8_t* out, void* stream);
  *   NVFP4_TUNE_GROUPED_STAGES  pipeline depth of the grouped kernel (2..16)
  *   NVFP4_TUNE_DENSE_KERNEL    large-M kernel: 1 single-CTA 128 x BN tiles, 2 CTA-pair
  *                              256 x 256 tiles (the default)
- *   NVFP4_TUNE_PDL             1: launch the decode-M and grouped kernels with programmatic
- *                              dependent launch, so their set-up overlaps the tail of the
- *                              previous kernel in the stream and the decode kernel requests
- *                              its first weight tiles before waiting for that kernel. Only
- *                              valid when the previous kernel does not write the weights
- *                              (b, sfb) of the call; activations, scales and outputs are
- *                              still ordered after it. 0 (default): plain stream order.
+ *   NVFP4_TUNE_PDL             programmatic dependent launch of the decode-M and grouped
+ *                              kernels. 2 (and 0, the default): their set-up (barriers, TMEM,
+ *                              descriptor prefetch) overlaps the tail of the previous kernel in
+ *                              the stream; every memory access waits for that kernel to
+ *                              complete, so stream order is kept in all cases. 1: in addition
+ *                              the decode kernel requests its first weight tiles before that
+ *                              wait; only valid when the previous kernel does not write the
+ *                              weights (b, sfb) of the call (activations, scales and outputs
+ *                              are still ordered after it). -1: plain stream order.
  * Returns NVFP4_OK or NVFP4_ERR_INVALID_ARG.
  */
 enum {

@@ -134,6 +134,10 @@ int encode_out(CUtensorMap* m, void* base, uint64_t rows, uint64_t cols) {
   return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+// Programmatic-dependent-launch mode of the streaming kernels: 0 off, 1 weights requested
+// before the dependency wait, 2 set-up overlap only (the default).
+int stream_pdl_mode() { return g_tune.pdl == 0 ? 2 : (g_tune.pdl < 0 ? 0 : g_tune.pdl); }
+
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
 
 int64_t pad16(int64_t v) { return (v + 15) / 16 * 16; }
@@ -207,7 +211,7 @@ int nvfp4_tune(int key, int value) {
       g_tune.dense_kernel = value;
       return NVFP4_OK;
     case NVFP4_TUNE_PDL:
-      if (value < 0 || value > 1) return NVFP4_ERR_INVALID_ARG;
+      if (value < -1 || value > 2) return NVFP4_ERR_INVALID_ARG;
       g_tune.pdl = value;
       return NVFP4_OK;
 
@@ -329,7 +333,7 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
     }
     if (split > KB) split = KB;
     s.split = split;
-    s.pdl = g_tune.pdl;
+    s.pdl = stream_pdl_mode();
     const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0) - 1536;
     const int recv_bytes = stream_recv_bytes(s.M, split);
     int stages = g_tune.stream_stages;
@@ -477,7 +481,7 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   s.N = static_cast<int>(N);
   s.K = static_cast<int>(K);
   s.split = 1;
-  s.pdl = g_tune.pdl;
+  s.pdl = stream_pdl_mode();
   s.x_rows = kGroupTileRows;
   s.acc_cols = kGroupTileRows;
   s.acc_bufs = 2;

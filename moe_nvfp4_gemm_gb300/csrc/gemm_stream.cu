@@ -200,7 +200,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
       if (mine > 0) mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>(S * mine * 512));
     }
     const Src src = item_src(first_it);
-    for (int j = 0; j < n_pre; ++j) issue_stage(j, first_it.kb0 + j, src, !p.pdl, false, 0, 0);
+    if (p.pdl == 2) griddep_wait();  // set-up-only overlap: no load before the previous kernel completes
+    for (int j = 0; j < n_pre; ++j) issue_stage(j, first_it.kb0 + j, src, p.pdl != 1, false, 0, 0);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, p.tmem_cols);
@@ -245,7 +246,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     // Dense path under a programmatic dependency: the first ring of weight tiles is
     // requested before waiting for the previous kernel; the token tiles (which that
     // kernel may have produced) only after it.
-    bool pending = !GROUPED && p.pdl;
+    bool pending = !GROUPED && p.pdl == 1;
+    if (p.pdl == 2) griddep_wait();
     int pend_stage[16], pend_kb[16], npend = 0;
     Item it;
     for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it) && !*abort_flag; i += stride) {

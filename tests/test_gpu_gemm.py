@@ -149,16 +149,20 @@ def test_empty_m_is_noop():
     m.nvfp4_gemm(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, 0, 128, 256, y=y)
 
 
-def test_programmatic_dependent_launch_keeps_stream_order():
-    # Back-to-back decode calls with programmatic dependent launch inside one CUDA graph,
+@pytest.mark.parametrize("pdl", [1, 2, -1])
+def test_programmatic_dependent_launch_keeps_stream_order(pdl):
+    # Back-to-back decode calls with programmatic dependent launch inside one CUDA graph
+    # (1: weights requested before the dependency wait, 2: set-up overlap only, the
+    # default; -1: plain stream order),
     # alternating between two problems: (1) each writing its own output must produce the
     # problem's own result; (2) all writing the same output, the last call's result must
     # win (every output write is ordered after the previous call's completion).
     A1, B1 = dense_case(16, 512, 1024, 31, 1.0, 1e-3, 0.02)
     A2, B2 = dense_case(16, 512, 1024, 32, 1.0, 1e-3, 0.02)
+    m.nvfp4_tune(m.NVFP4_TUNE_PDL, -1)
     ref1 = _run(A1, B1).clone()
     ref2 = _run(A2, B2).clone()
-    m.nvfp4_tune(m.NVFP4_TUNE_PDL, 1)
+    m.nvfp4_tune(m.NVFP4_TUNE_PDL, pdl)
     calls = [(A1, B1), (A2, B2)] * 4 + [(A1, B1)]
     outs = [torch.empty_like(ref1) for _ in calls]
     y = torch.empty_like(ref1)
