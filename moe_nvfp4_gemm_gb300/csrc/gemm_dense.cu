@@ -293,6 +293,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
   if (warp == 0) {
     const uint64_t pol = policy_evict_last();
+    griddep_wait();  // launched as a programmatic dependent: loads wait for the previous kernel
     int s = 0;
     uint32_t ph = 0;
     int issued_phase[STAGES];
@@ -321,6 +322,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         }
       }
     }
+    griddep_launch_dependents();  // this CTA's loads are all issued: let the next kernel set up
     // The even CTA's full barriers count both CTAs' bytes: let them all land.
     if (leader)
       for (int i = 0; i < STAGES; ++i)
@@ -404,6 +406,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
   } else {
     const int q = warp & 3, h = (warp - 2) >> 2;
+    griddep_wait();  // reads the global scales, writes y
     const float alpha = __ldg(p.ga) * __ldg(p.gb);
     uint8_t* buf = out_buf + (warp - 2) * 4096;
     const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
@@ -523,13 +526,17 @@ cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, co
   cfg.blockDim = dim3(kPairThreads);
   cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch, set-up only: barrier and TMEM set-up and descriptor
+  // prefetch overlap the previous kernel's tail; every memory access waits for it
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmSFA, tmSFB, tmY, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

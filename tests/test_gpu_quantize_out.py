@@ -57,3 +57,40 @@ def test_quantized_output_rejects_n_not_multiple_of_64():
     A, B = dense_case(128, 136, 256, 52)
     with pytest.raises(m.NVFP4Error):
         m.nvfp4_gemm_quantize_out(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, scalar(np.float32(1.0)), 128, 136, 256)
+
+
+def test_chained_layers_keep_stream_order():
+    # layer 1 emits NVFP4 that layer 2 reads as its activations, back to back in one CUDA
+    # graph (both launches overlap their set-up with the previous kernel): the result must
+    # equal the same chain run with a synchronisation between the layers, and writing the
+    # same output twice must leave the last call's values
+    A, B1 = dense_case(512, 512, 1024, 53, 1.0, 1e-3, 0.05)
+    _, B2 = dense_case(512, 768, 512, 54, 1.0, 1e-3, 0.05)
+    g1 = scalar(np.float32(2.0 ** -5))
+    q1, sf1 = m.nvfp4_gemm_quantize_out(A.dq, A.dsf, A.dg, B1.dq, B1.dsf, B1.dg, g1, 512, 512, 1024)
+    torch.cuda.synchronize()
+    ref = m.nvfp4_gemm(q1, sf1, g1, B2.dq, B2.dsf, B2.dg, 512, 768, 512).clone()
+    torch.cuda.synchronize()
+    q = torch.empty_like(q1)
+    sf = torch.empty_like(sf1)
+    y = torch.empty_like(ref)
+    y_other = torch.empty_like(ref)
+    y_mid = torch.empty((512, 512), dtype=torch.bfloat16, device=dev())
+
+    def chain():
+        m.nvfp4_gemm_quantize_out(A.dq, A.dsf, A.dg, B1.dq, B1.dsf, B1.dg, g1, 512, 512, 1024, q_out=q, sf_out=sf)
+        m.nvfp4_gemm(q, sf, g1, B2.dq, B2.dsf, B2.dg, 512, 768, 512, y=y_other)  # overwritten next
+        m.nvfp4_gemm(A.dq, A.dsf, A.dg, B1.dq, B1.dsf, B1.dg, 512, 512, 1024, y=y_mid)
+        m.nvfp4_gemm(q, sf, g1, B2.dq, B2.dsf, B2.dg, 512, 768, 512, y=y)
+
+    chain()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        chain()
+    q.zero_()
+    y.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(q, q1) and torch.equal(sf, sf1)
+    assert torch.equal(y, ref)
