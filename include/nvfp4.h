@@ -148,6 +148,26 @@ int nvfp4_grouped_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, co
                        size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * Grouped GEMM with the token gather fused into its load stage: routed row r (rows sorted
+ * by expert as in nvfp4_grouped_gemm) multiplies token row_token[r] of the T-row
+ * activations, so tokens are quantised once and never permuted in memory ("The Moment
+ * of Synthesis", magik.net, Reasoning: top-8 routing sends each token to 8 experts).
+ *   a_tok, sfa_tok   activations [T, K/2] and their tiled scales over T rows
+ *   row_token        device int32 [M_total], values in [0, T); a value outside it is
+ *                    reported as NVFP4_ERR_BAD_OFFSETS in *dev_status (its row's output is
+ *                    then unspecified; nothing is read out of bounds)
+ *   y                bf16 [M_total, N], routed-row order
+ * Other arguments and the workspace as nvfp4_grouped_gemm. Rows are fetched with TMA
+ * tile::gather4 (four token rows per instruction); the result equals nvfp4_grouped_gemm
+ * on the gathered rows bit for bit.
+ */
+int nvfp4_grouped_gemm_gather(const uint8_t* a_tok, const uint8_t* sfa_tok, const float* ga, const uint8_t* b,
+                              const uint8_t* sfb, const float* gb, const int32_t* expert_offsets,
+                              const int32_t* row_token, int32_t E, int64_t T, int64_t M_total, int64_t N, int64_t K,
+                              uint16_t* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              void* stream);
+
+/*
  * MoE gate/up projection with the SwiGLU activation fused into the epilogue:
  * y[m, c] = silu(gate[m, c]) * up[m, c], silu(v) = v / (1 + exp(-v)), where gate and
  * up are the grouped GEMM's outputs for expert e's weight rows 2c and 2c + 1

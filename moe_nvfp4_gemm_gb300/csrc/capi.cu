@@ -430,11 +430,13 @@ size_t nvfp4_grouped_gemm_workspace_bytes(int32_t E, int64_t M_total, int64_t N,
   return static_cast<size_t>(grouped_slab_offset(E, M_total) + grouped_max_tiles(E, M_total) * (K / 64) * 512);
 }
 
+// row_token (null: none): routed row r reads row row_token[r] of the T-row activations a.
 static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b, const uint8_t* sfb,
                         const float* gb, const int32_t* expert_offsets, int32_t E, int64_t M_total, int64_t N,
                         int64_t K, uint16_t* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                        void* stream, int swiglu) {
+                        void* stream, int swiglu, const int32_t* row_token = nullptr, int64_t T = 0) {
   g_last_launches = 0;
+  if (row_token && M_total > 0 && (T <= 0 || T > kMaxDim)) return NVFP4_ERR_INVALID_ARG;
   if (E <= 0) return NVFP4_ERR_INVALID_ARG;
   int rc = check_gemm_shape(M_total, N, K);
   if (rc) return rc;
@@ -459,15 +461,22 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   int prep_grid = static_cast<int>((words + 255) / 256);
   if (prep_grid > 4 * d.sms) prep_grid = 4 * d.sms;
   if (prep_grid < 1) prep_grid = 1;
-  rc = from_cuda(launch_grouped_prep(expert_offsets, E, static_cast<int>(M_total), static_cast<int>(K), sfa, n_tiles,
+  rc = from_cuda(launch_grouped_prep(expert_offsets, row_token, static_cast<int>(T), E, static_cast<int>(M_total),
+                                     static_cast<int>(K), sfa, n_tiles,
                                      tiles, slabs, dev_status, prep_grid, st));
   g_last_launches = 1;
   if (rc) return rc;
 
   CUtensorMap tmW, tmX;
   if ((rc = encode_2d(&tmW, b, static_cast<uint64_t>(E) * N, K / 2, 128))) return rc;
-  if ((rc = encode_2d(&tmX, a, M_total, K / 2, 16))) return rc;
+  if (row_token) {
+    if ((rc = encode_2d(&tmX, a, T, K / 2, 1))) return rc;  // one-row boxes for tile::gather4
+  } else if ((rc = encode_2d(&tmX, a, M_total, K / 2, 16))) {
+    return rc;
+  }
   StreamArgs s = {};
+  s.row_token = row_token;
+  s.T = static_cast<int>(T);
   s.sfw = sfb;
   s.sfw_stride = nvfp4_scale_bytes(N, K);
   s.sfx = slabs;
@@ -488,11 +497,11 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   s.swiglu = swiglu;
   const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0) - 1536;
   int stages = g_tune.grouped_stages;
-  if (stages == 0) stages = (kSmemLimit - 1536) / stage_bytes;
+  if (stages == 0) stages = (kSmemLimit - 1536 - 256) / stage_bytes;
   const int tmem_room = (512 - 2 * s.acc_cols) / 32;
   if (stages > tmem_room) stages = tmem_room;
   if (stages > 16) stages = 16;
-  if (stream_smem_bytes(stages, s.x_rows, 0) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (stream_smem_bytes(stages, s.x_rows, 256) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   s.stages = stages;
   s.tmem_cols = pow2_at_least(2 * s.acc_cols + 32 * stages);
   const int grid = g_tune.grouped_grid ? g_tune.grouped_grid : d.sms;
@@ -507,6 +516,16 @@ int nvfp4_grouped_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, co
                        void* stream) {
   return grouped_impl(a, sfa, ga, b, sfb, gb, expert_offsets, E, M_total, N, K, y, workspace, workspace_bytes,
                       dev_status, stream, 0);
+}
+
+int nvfp4_grouped_gemm_gather(const uint8_t* a_tok, const uint8_t* sfa_tok, const float* ga, const uint8_t* b,
+                              const uint8_t* sfb, const float* gb, const int32_t* expert_offsets,
+                              const int32_t* row_token, int32_t E, int64_t T, int64_t M_total, int64_t N, int64_t K,
+                              uint16_t* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              void* stream) {
+  if (!row_token && M_total > 0) return NVFP4_ERR_INVALID_ARG;
+  return grouped_impl(a_tok, sfa_tok, ga, b, sfb, gb, expert_offsets, E, M_total, N, K, y, workspace, workspace_bytes,
+                      dev_status, stream, 0, row_token, T);
 }
 
 int nvfp4_grouped_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b_gu,

@@ -112,6 +112,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_bar + 3);
   volatile uint32_t* policies_ready = tmem_slot + 2;
   float* recv = reinterpret_cast<float*>(smem + STAGES * L.stage_bytes + 512);
+  // grouped with a token gather: the x rows (token indices) of the producer's current item
+  int32_t* tok_idx = reinterpret_cast<int32_t*>(smem + STAGES * L.stage_bytes + 512);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -155,13 +157,20 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
       tma_load_2d_plain(st, &tmW, bar, kb * 128, wrow0);
       bulk_load_plain(st + L.sfw_off, sfw + kb * 2048, nsub * 512, bar);
     }
-    if (with_x) {
+    if (with_x && GROUPED && p.row_token) {
+      // token gather: four rows per instruction from the one-row-box map of x
+      for (int j = 0; j < n16 * 4; ++j)
+        tma_gather4(st + L.x_off + j * 512, &tmX, bar, kb * 128, tok_idx[4 * j], tok_idx[4 * j + 1],
+                    tok_idx[4 * j + 2], tok_idx[4 * j + 3]);
+    } else if (with_x) {
       for (int j = 0; j < n16; ++j) {
         if (hint)
           tma_load_2d(st + L.x_off + j * 2048, &tmX, bar, kb * 128, src.row0 + j * 16, pol_x);
         else
           tma_load_2d_plain(st + L.x_off + j * 2048, &tmX, bar, kb * 128, src.row0 + j * 16);
       }
+    }
+    if (with_x) {
       if (hint)
         bulk_load(st + L.sfx_off, sfx + kb * 2048, nsub * 512, bar, pol_x);
       else
@@ -250,10 +259,28 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     if (p.pdl == 2) griddep_wait();
     int pend_stage[16], pend_kb[16], npend = 0;
     Item it;
+    auto load_tokens = [&](const Item& x) {
+      return make_int2(__ldg(p.row_token + x.row0 + min(lane, x.rows - 1)),
+                       __ldg(p.row_token + x.row0 + min(lane + 32, x.rows - 1)));
+    };
+    int2 tok_regs = make_int2(0, 0);
+    bool tok_ready = false;
     for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it) && !*abort_flag; i += stride) {
       const Src src = item_src(it);
       const int n16 = src.n16;
       const uint8_t* sfx = src.sfx;
+      if (GROUPED && p.row_token) {
+        // this item's token rows (loaded during the previous item, two per lane); rows past
+        // the tile's count repeat its last row (their accumulator columns are never stored),
+        // indices clamped into x (prep reports bad ones)
+        if (!tok_ready) tok_regs = load_tokens(it);
+        tok_idx[lane] = min(max(tok_regs.x, 0), p.T - 1);
+        tok_idx[lane + 32] = min(max(tok_regs.y, 0), p.T - 1);
+        __syncwarp();
+        Item nx;  // start the next item's index loads now; they land while this item streams
+        tok_ready = get_item<GROUPED>(p, i + stride, n_items, NT, KB, nx);
+        if (tok_ready) tok_regs = load_tokens(nx);
+      }
       for (int kb = it.kb0; kb < it.kb1; ++kb) {
         if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag)) break;
         if (!have_pol && issued >= STAGES && *policies_ready) {
@@ -520,8 +547,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
 // expert each; experts without rows get none) and gathers each tile's token
 // scales into its own slab in the 128-row tiled layout, rows starting at 0.
 // Workspace: [0] n_tiles, [16..) int4 tiles[max_tiles], then the slabs.
-__global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict__ offsets, int E, int M_total, int K,
-                                                      const uint8_t* __restrict__ sfx, int32_t* n_tiles_out,
+__global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict__ offsets,
+                                                      const int32_t* __restrict__ row_token, int T, int E, int M_total,
+                                                      int K, const uint8_t* __restrict__ sfx, int32_t* n_tiles_out,
                                                       int4* __restrict__ tiles, uint8_t* __restrict__ slabs,
                                                       int32_t* status) {
   extern __shared__ int32_t sh[];  // offsets[E+1], tile_base[E+1]
@@ -577,8 +605,16 @@ __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict_
     const int j = m - off[lo];
     const int tile = tbase[lo] + j / kGroupTile;
     const int r = j % kGroupTile;
-    const uint32_t v = *reinterpret_cast<const uint32_t*>(sfx + ((m / 128) * KC4 + c4) * 512 + (m % 32) * 16 +
-                                                          ((m % 128) / 32) * 4);
+    int src = m;  // the row of x (and of its scales) this routed row reads
+    if (row_token) {
+      src = __ldg(row_token + m);
+      if (src < 0 || src >= T) {  // reported, and clamped so that nothing is read out of bounds
+        if (c4 == 0) report_status(status, kStatusBadOffsets);
+        src = src < 0 ? 0 : T - 1;
+      }
+    }
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(sfx + ((src / 128) * KC4 + c4) * 512 + (src % 32) * 16 +
+                                                          ((src % 128) / 32) * 4);
     *reinterpret_cast<uint32_t*>(slabs + (tile * KC4 + c4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4) = v;
   }
 }
@@ -588,7 +624,8 @@ __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict_
 template <bool GROUPED>
 static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, int grid,
                                    cudaStream_t st) {
-  const int smem = stream_smem_bytes(a.stages, a.x_rows, GROUPED ? 0 : stream_recv_bytes(a.M, a.split));
+  // grouped: 256 bytes of token indices (the token gather); dense: the reduction's receive area
+  const int smem = stream_smem_bytes(a.stages, a.x_rows, GROUPED ? 256 : stream_recv_bytes(a.M, a.split));
   cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_gemm_stream<GROUPED>));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -629,7 +666,8 @@ cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const 
   return grouped ? launch_stream_t<true>(tmW, tmX, a, grid, st) : launch_stream_t<false>(tmW, tmX, a, grid, st);
 }
 
-cudaError_t launch_grouped_prep(const int32_t* offsets, int E, int M_total, int K, const uint8_t* sfx,
+cudaError_t launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int T, int E, int M_total, int K,
+                                const uint8_t* sfx,
                                 int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
                                 cudaStream_t st) {
   const int smem = 2 * (E + 1) * 4;
@@ -637,7 +675,7 @@ cudaError_t launch_grouped_prep(const int32_t* offsets, int E, int M_total, int 
     cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_grouped_prep));
     if (e != cudaSuccess) return e;
   }
-  k_grouped_prep<<<grid, 256, smem, st>>>(offsets, E, M_total, K, sfx, n_tiles, tiles, slabs, status);
+  k_grouped_prep<<<grid, 256, smem, st>>>(offsets, row_token, T, E, M_total, K, sfx, n_tiles, tiles, slabs, status);
   return cudaGetLastError();
 }
 

@@ -42,6 +42,8 @@ struct StreamArgs {
   int tmem_cols;
   int pdl;                 // launched with programmatic stream serialization
   int swiglu;              // grouped: weight rows interleave gate/up; y[t, c] = silu(gate) * up, N / 2 wide
+  const int32_t* row_token;  // grouped: routed row r reads token row row_token[r] of x (null: row r)
+  int T;                     // grouped with row_token: rows of x
 };
 
 
@@ -59,7 +61,8 @@ cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, co
                               cudaStream_t st, bool quantized_out = false);
 cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, bool grouped,
                           int grid, cudaStream_t st);
-cudaError_t launch_grouped_prep(const int32_t* offsets, int E, int M_total, int K, const uint8_t* sfx,
+cudaError_t launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int T, int E, int M_total, int K,
+                                const uint8_t* sfx,
                                 int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
                                 cudaStream_t st);
 int stream_smem_bytes(int stages, int x_rows, int recv_bytes);

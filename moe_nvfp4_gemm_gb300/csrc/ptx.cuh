@@ -181,6 +181,17 @@ DEVI void bulk_load_plain(void* dst, const void* src, uint32_t bytes, uint64_t* 
                : "memory");
 }
 
+// Four rows (r0..r3) of a 2-D tensor whose map has a one-row box, `x` the first
+// column: 4 x box-width bytes land contiguously at dst (swizzled like a tile load).
+DEVI void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t x, int32_t r0, int32_t r1, int32_t r2,
+                      int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+      : "memory");
+}
+
 // Bulk copy from this CTA's shared memory into another CTA's of the cluster, completing
 // `bytes` on the mbarrier at `bar_cluster` there; tracked by this thread's bulk group.
 DEVI void bulk_copy_to_cluster(uint32_t dst_cluster, const void* src, uint32_t bytes, uint32_t bar_cluster) {

@@ -186,3 +186,67 @@ def test_grouped_swiglu_moe_workload_sampled():
     cols = np.concatenate([[0, 63, 64, 2047], rng.choice(2048, 40, replace=False)])
     g.check_swiglu(y, rows=rows, cols=cols)
 
+
+
+def _gathered(qa_tok, sfa_tok, T, K, row_token):
+    """The routed-row operands a plain grouped GEMM would take: packed rows and block
+    scales gathered by token (blocks run along K, so gathering commutes with quantising)."""
+    Mt = len(row_token)
+    qa = np.ascontiguousarray(qa_tok[row_token])
+    sfa = oracle.sf_swizzle(oracle.sf_unswizzle(sfa_tok, T, K)[row_token], Mt, K)
+    return qa, sfa
+
+
+@pytest.mark.parametrize("T,counts,N,K", [
+    (37, (3, 0, 17, 1, 0, 9), 256, 512),
+    (200, (64, 65, 1, 70, 0), 136, 1088),
+    (5, (40,), 256, 256),                  # more routed rows than tokens: tokens repeat
+])
+def test_grouped_gather_matches_gathered_plain_and_oracle(T, counts, N, K):
+    rng = np.random.default_rng(T)
+    Mt = int(sum(counts))
+    row_token = rng.integers(0, T, size=Mt).astype(np.int32)
+    qa_tok, sfa_tok, ga = oracle.quantize(synth.normal_bf16((T, K), 61, 1.0, 1e-3))
+    qa, sfa = _gathered(qa_tok, sfa_tok, T, K, row_token)
+    g = Grouped(counts, N, K, 62)
+    g.qa, g.sfa, g.ga = qa, sfa, ga
+    y_plain = g.run()
+    y = m.nvfp4_grouped_gemm_gather(to_dev(qa_tok), to_dev(sfa_tok), scalar(ga), to_dev(g.qb), to_dev(g.sfb),
+                                    to_dev(g.gb), to_dev(g.off), to_dev(row_token), g.E, T, Mt, N, K)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_plain)
+    g.check(y)
+
+
+def test_grouped_gather_moe_workload():
+    # 512 tokens quantised once, routed top-8 over 256 experts (4096 rows), K = 6144, N = 4096
+    T, K, N = 512, 6144, 4096
+    tok, _, off = synth.route_topk(T, 256, 8, 1003)
+    qa_tok, sfa_tok, ga = oracle.quantize(synth.normal_bf16((T, K), 6, 1.0))
+    qa, sfa = _gathered(qa_tok, sfa_tok, T, K, tok.astype(np.int64))
+    counts = np.diff(off)
+    gg = Grouped(tuple(counts), N, K, 3, a_rows=synth.normal_bf16((int(off[-1]), K), 6, 1.0),
+                 w=lambda e: synth.moe_expert_weight(e, N, K, 3))
+    gg.qa, gg.sfa, gg.ga = qa, sfa, ga
+    y_plain = gg.run()
+    y = m.nvfp4_grouped_gemm_gather(to_dev(qa_tok), to_dev(sfa_tok), scalar(ga), to_dev(gg.qb), to_dev(gg.sfb),
+                                    to_dev(gg.gb), to_dev(gg.off), to_dev(tok.astype(np.int32)), 256, T,
+                                    int(off[-1]), N, K)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_plain)
+    rng = np.random.default_rng(5)
+    rows = np.concatenate([[0, gg.Mt - 1], rng.choice(gg.Mt, 20, replace=False)])
+    cols = np.concatenate([[0, 4095], rng.choice(4096, 30, replace=False)])
+    gg.check(y, rows=rows, cols=cols)
+
+
+def test_grouped_gather_bad_token_index_reported():
+    T, K, N = 16, 256, 128
+    qa_tok, sfa_tok, ga = oracle.quantize(synth.normal_bf16((T, K), 63, 1.0))
+    g = Grouped((4, 4), N, K, 64)
+    row_token = np.array([0, 1, 2, 3, 4, 5, 16, 7], dtype=np.int32)  # 16 is out of range
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    m.nvfp4_grouped_gemm_gather(to_dev(qa_tok), to_dev(sfa_tok), scalar(ga), to_dev(g.qb), to_dev(g.sfb),
+                                to_dev(g.gb), to_dev(g.off), to_dev(row_token), g.E, T, 8, N, K, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == -8
