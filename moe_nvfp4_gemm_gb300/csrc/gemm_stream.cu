@@ -86,7 +86,9 @@ constexpr int kStreamWaiterWarp = 6;
 constexpr uint32_t kStreamHandoffBarrier = 1;
 constexpr uint32_t kStreamEpilogueBarrier = 2;  // the 4 epilogue warps
 
-template <bool GROUPED>
+// VARIANT (grouped only): bit 0 SwiGLU epilogue, bit 1 token gather in the load stage;
+// compiled separately so that the plain grouped kernel carries neither.
+template <bool GROUPED, int VARIANT = 0>
 __global__ void __launch_bounds__(kStreamThreads, 2)
     k_gemm_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                   const StreamArgs p) {
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
       tma_load_2d_plain(st, &tmW, bar, kb * 128, wrow0);
       bulk_load_plain(st + L.sfw_off, sfw + kb * 2048, nsub * 512, bar);
     }
-    if (with_x && GROUPED && p.row_token) {
+    if (with_x && GROUPED && (VARIANT & 2)) {
       // token gather: four rows per instruction from the one-row-box map of x
       for (int j = 0; j < n16 * 4; ++j)
         tma_gather4(st + L.x_off + j * 512, &tmX, bar, kb * 128, tok_idx[4 * j], tok_idx[4 * j + 1],
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
       const Src src = item_src(it);
       const int n16 = src.n16;
       const uint8_t* sfx = src.sfx;
-      if (GROUPED && p.row_token) {
+      if (GROUPED && (VARIANT & 2)) {
         // this item's token rows (loaded during the previous item, two per lane); rows past
         // the tile's count repeat its last row (their accumulator columns are never stored),
         // indices clamped into x (prep reports bad ones)
@@ -440,7 +442,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         __syncwarp();
         if (elect_one()) mbar_arrive(&tempty[buf]);
         __syncwarp();
-        if (p.swiglu) {
+        if (VARIANT & 1) {
           // Weight rows 2c and 2c + 1 (gate and up of output column c) sit in adjacent
           // lanes: the even lane takes its partner's value and writes silu(gate) * up.
           const int n_out = N >> 1;
@@ -621,12 +623,12 @@ __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict_
 
 // ---- host launchers -------------------------------------------------------------------
 
-template <bool GROUPED>
+template <bool GROUPED, int VARIANT>
 static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, int grid,
                                    cudaStream_t st) {
   // grouped: 256 bytes of token indices (the token gather); dense: the reduction's receive area
   const int smem = stream_smem_bytes(a.stages, a.x_rows, GROUPED ? 256 : stream_recv_bytes(a.M, a.split));
-  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_gemm_stream<GROUPED>));
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_gemm_stream<GROUPED, VARIANT>));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -649,7 +651,7 @@ static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tm
   }
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
-  e = cudaLaunchKernelEx(&cfg, k_gemm_stream<GROUPED>, tmW, tmX, a);
+  e = cudaLaunchKernelEx(&cfg, k_gemm_stream<GROUPED, VARIANT>, tmW, tmX, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -663,7 +665,11 @@ int stream_smem_bytes(int stages, int x_rows, int recv_bytes) {
 
 cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, bool grouped, int grid,
                           cudaStream_t st) {
-  return grouped ? launch_stream_t<true>(tmW, tmX, a, grid, st) : launch_stream_t<false>(tmW, tmX, a, grid, st);
+  if (!grouped) return launch_stream_t<false, 0>(tmW, tmX, a, grid, st);
+  if (a.row_token && a.swiglu) return cudaErrorInvalidValue;  // no entry point combines them
+  if (a.row_token) return launch_stream_t<true, 2>(tmW, tmX, a, grid, st);
+  if (a.swiglu) return launch_stream_t<true, 1>(tmW, tmX, a, grid, st);
+  return launch_stream_t<true, 0>(tmW, tmX, a, grid, st);
 }
 
 cudaError_t launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int T, int E, int M_total, int K,
