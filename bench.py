@@ -542,6 +542,26 @@ def run_decode(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
                                            "us_pdl: weights also requested before the wait (static weights); "
                                            "us_plain_stream_order: no overlap",
                                "us_plain_stream_order": ms_plain * 1e3}
+        if M in (1, 16):
+            # L2 retention: one hot weight (the original matrix) called between four calls on
+            # the rotating copies (151 MB streamed per step); hot-call time = step - cold-only step
+            def step(i, keep):
+                if keep is not None:
+                    m.nvfp4_tune(m.NVFP4_TUNE_WEIGHT_L2, keep)
+                    m.nvfp4_gemm(xa, sfa, ga, wq, sfw, gw, M, SQ, SQ, y=y)
+                m.nvfp4_tune(m.NVFP4_TUNE_WEIGHT_L2, 0)
+                for j in range(4):
+                    c = copies[(4 * i + j) % 8]
+                    m.nvfp4_gemm(xa, sfa, ga, c[0], c[1], gw, M, SQ, SQ, y=y)
+            ms_cold = time_graph(lambda i: step(i, None), 8, 20, stream)
+            ms_streamed = time_graph(lambda i: step(i, 0), 8, 20, stream) - ms_cold
+            ms_kept = time_graph(lambda i: step(i, 1), 8, 20, stream) - ms_cold
+            out[f"decode_l2_kept_M{M}"] = {
+                "us_hot_call_kept": ms_kept * 1e3, "us_hot_call_streamed": ms_streamed * 1e3,
+                "us_cold_step": ms_cold * 1e3,
+                "timing": "CUDA graph of 8 steps; a step = hot-weight call + 4 calls on rotating copies; "
+                          "hot-call time = step time - cold-only step time",
+                "note": "kept: hot weight loaded L2 evict_last (NVFP4_TUNE_WEIGHT_L2=1), cold ones evict_first"}
     del copies, wq, sfw
 
 

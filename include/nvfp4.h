@@ -249,6 +249,15 @@ int nvfp4_encode_e4m3(const float* v, int64_t n, uint8_t* out, void* stream);
  *                              wait; only valid when the previous kernel does not write the
  *                              weights (b, sfb) of the call (activations, scales and outputs
  *                              are still ordered after it). -1: plain stream order.
+ *   NVFP4_TUNE_WEIGHT_L2       L2 residency of the weights (b, sfb) read by the decode-M and
+ *                              grouped kernels. 0 (default): streamed, loaded with the
+ *                              evict_first priority so a read-once matrix displaces nothing.
+ *                              1: kept, loaded with the evict_last priority, so a matrix that
+ *                              fits in L2 and is called again stays resident while other
+ *                              weights stream past it (the "L2 cache pinning" of magik.net,
+ *                              "The Moment of Recalibration", The Broader Narrative Arc). Lines
+ *                              keep the priority they were last loaded with; a later call with
+ *                              0 on the same matrix demotes them again. Results are unchanged.
  * Returns NVFP4_OK or NVFP4_ERR_INVALID_ARG.
  */
 enum {
@@ -260,7 +269,8 @@ enum {
   NVFP4_TUNE_GROUPED_GRID = 6,
   NVFP4_TUNE_GROUPED_STAGES = 7,
   NVFP4_TUNE_DENSE_KERNEL = 8,
-  NVFP4_TUNE_PDL = 9
+  NVFP4_TUNE_PDL = 9,
+  NVFP4_TUNE_WEIGHT_L2 = 10
 };
 int nvfp4_tune(int key, int value);
 

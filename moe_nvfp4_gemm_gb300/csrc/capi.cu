@@ -44,7 +44,7 @@ thread_local int g_last_launches = 0;
 
 struct Tune {
   int dense_bn = 0, dense_grid = 0, stream_max_m = 0, stream_split = 0, stream_stages = 0, grouped_grid = 0,
-      grouped_stages = 0, dense_kernel = 0, pdl = 0;
+      grouped_stages = 0, dense_kernel = 0, pdl = 0, weight_l2 = 0;
 } g_tune;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -214,6 +214,10 @@ int nvfp4_tune(int key, int value) {
       if (value < -1 || value > 2) return NVFP4_ERR_INVALID_ARG;
       g_tune.pdl = value;
       return NVFP4_OK;
+    case NVFP4_TUNE_WEIGHT_L2:
+      if (value < 0 || value > 1) return NVFP4_ERR_INVALID_ARG;
+      g_tune.weight_l2 = value;
+      return NVFP4_OK;
 
     default:
       return NVFP4_ERR_INVALID_ARG;
@@ -334,6 +338,7 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
     if (split > KB) split = KB;
     s.split = split;
     s.pdl = stream_pdl_mode();
+    s.w_keep = g_tune.weight_l2;
     const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0) - 1536;
     const int recv_bytes = stream_recv_bytes(s.M, split);
     int stages = g_tune.stream_stages;
@@ -491,6 +496,7 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   s.K = static_cast<int>(K);
   s.split = 1;
   s.pdl = stream_pdl_mode();
+  s.w_keep = g_tune.weight_l2;
   s.x_rows = kGroupTileRows;
   s.acc_cols = kGroupTileRows;
   s.acc_bufs = 2;

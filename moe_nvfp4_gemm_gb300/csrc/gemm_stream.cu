@@ -211,8 +211,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
       if (mine > 0) mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>(S * mine * 512));
     }
     const Src src = item_src(first_it);
+    // Weights kept in L2: the first ring carries the evict_last hint as well (its policy
+    // costs this thread ~0.6 us), so that none of the matrix is left at normal priority.
+    const uint64_t keep = p.w_keep ? policy_evict_last() : 0;
     if (p.pdl == 2) griddep_wait();  // set-up-only overlap: no load before the previous kernel completes
-    for (int j = 0; j < n_pre; ++j) issue_stage(j, first_it.kb0 + j, src, p.pdl != 1, false, 0, 0);
+    for (int j = 0; j < n_pre; ++j) issue_stage(j, first_it.kb0 + j, src, p.pdl != 1, p.w_keep != 0, keep, keep);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, p.tmem_cols);
@@ -405,7 +408,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   } else {
     constexpr int MAXC = kGroupTile;
     if (warp == 2) {
-      const uint64_t pw = policy_evict_first(), px = policy_evict_last();
+      // Weights are read once per call: evict_first keeps them from displacing the token
+      // tiles (evict_last) and other data, unless the caller asks to keep them in L2.
+      const uint64_t pw = p.w_keep ? policy_evict_last() : policy_evict_first(), px = policy_evict_last();
       if (lane == 0) {
         policies[0] = pw;
         policies[1] = px;

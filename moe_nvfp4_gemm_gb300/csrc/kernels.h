@@ -44,6 +44,7 @@ struct StreamArgs {
   int swiglu;              // grouped: weight rows interleave gate/up; y[t, c] = silu(gate) * up, N / 2 wide
   const int32_t* row_token;  // grouped: routed row r reads token row row_token[r] of x (null: row r)
   int T;                     // grouped with row_token: rows of x
+  int w_keep;                // weights loaded L2 evict_last (kept resident across calls), else evict_first
 };
 
 

@@ -94,3 +94,7 @@ def test_tune_rejects_bad_values(lib):
     assert lib.nvfp4_tune(4, 9) == -1
     assert lib.nvfp4_tune(99, 1) == -1
     assert lib.nvfp4_tune(1, 0) == 0
+    assert lib.nvfp4_tune(10, 2) == -1   # weight L2 residency: 0 streamed, 1 kept
+    assert lib.nvfp4_tune(10, -1) == -1
+    assert lib.nvfp4_tune(10, 1) == 0
+    assert lib.nvfp4_tune(10, 0) == 0

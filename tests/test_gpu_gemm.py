@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(autouse=True)
 def _reset_tuning():
     yield
-    for key in range(1, 10):
+    for key in range(1, 11):
         m.nvfp4_tune(key, 0)
 
 
@@ -147,6 +147,18 @@ def test_empty_m_is_noop():
     A, B = dense_case(1, 128, 256, 4)
     y = torch.full((0, 128), 7.0, dtype=torch.bfloat16, device=dev())
     m.nvfp4_gemm(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, 0, 128, 256, y=y)
+
+
+@pytest.mark.parametrize("M,split", [(1, 0), (16, 4), (77, 1)])
+def test_weights_kept_in_l2_give_identical_results(M, split):
+    # the weight loads' L2 priority (evict_first or evict_last) changes no arithmetic
+    A, B = dense_case(M, 384, 2048, 33, 1.0, 1e-3, 0.02)
+    m.nvfp4_tune(m.NVFP4_TUNE_STREAM_SPLIT, split)
+    streamed = _run(A, B).clone()
+    m.nvfp4_tune(m.NVFP4_TUNE_WEIGHT_L2, 1)
+    kept = _run(A, B)
+    assert torch.equal(kept.view(torch.int16), streamed.view(torch.int16))
+    check_gemm(kept, A, B)
 
 
 @pytest.mark.parametrize("pdl", [1, 2, -1])

@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(autouse=True)
 def _reset_tuning():
     yield
-    for key in range(1, 10):
+    for key in range(1, 11):
         m.nvfp4_tune(key, 0)
 
 
@@ -90,6 +90,15 @@ def test_grouped_ragged_counts(counts):
 def test_grouped_ragged_n_and_k():
     g = Grouped((10, 40, 0, 7), 136, 1088, 22)
     g.check(g.run())
+
+
+def test_grouped_weights_kept_in_l2_identical():
+    g = Grouped((10, 40, 0, 7, 70), 256, 1024, 24)
+    streamed = g.run().clone()
+    m.nvfp4_tune(m.NVFP4_TUNE_WEIGHT_L2, 1)
+    kept = g.run()
+    assert torch.equal(kept.view(torch.int16), streamed.view(torch.int16))
+    g.check(kept)
 
 
 def test_grouped_small_persistent_grid_and_stages():
