@@ -476,9 +476,11 @@ def time_launches(fn, n, stream, warm=3):
     return statistics.median(a.elapsed_time(b) for a, b in ev)
 
 
-def time_graph(fn, calls, reps, stream):
+def time_graph(fn, calls, reps, stream, trials=3):
     """Device time (ms) per fn() call: `calls` calls captured in one CUDA graph, replayed
-    `reps` times between two events (host launch overhead excluded)."""
+    `reps` times between two events (host launch overhead excluded); the median of
+    `trials` such loops, so that one loop whose replays the host enqueued late (the
+    events then time an idle GPU) does not decide the figure."""
     import torch
     for i in range(3):
         fn(i)
@@ -489,13 +491,16 @@ def time_graph(fn, calls, reps, stream):
             fn(i)
     g.replay()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(reps):
-        g.replay()
-    b.record(stream)
-    torch.cuda.synchronize()
-    return a.elapsed_time(b) / (calls * reps)
+    per_call = []
+    for _ in range(trials):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        per_call.append(a.elapsed_time(b) / (calls * reps))
+    return statistics.median(per_call)
 
 
 def run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak, only=None):
