@@ -598,15 +598,23 @@ def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
     gbs = mbytes / (ms * 1e-3) / 1e9
     out["moe_grouped"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
                           "bytes": mbytes, "tflops": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12}
-    # the same tokens quantised once (512 rows) and gathered by the grouped GEMM's loads
+    # the same tokens quantised once (512 rows) and gathered by routed row: copied out by the
+    # preparation kernel (default workspace), or fetched by the GEMM's load stage (plain-size
+    # workspace)
     xq_t, sf_t, g_t = quantize_dev(to_dev(synth.normal_bf16((512, K), 2 * 3, 1.0)))
     tok_d = torch.from_numpy(np.ascontiguousarray(tok.astype(np.int32))).to(dev)
+    wsg = torch.empty(m.nvfp4_grouped_gemm_gather_workspace_bytes(E, Mt, N, K), dtype=torch.uint8, device=dev)
     ms = time_graph(lambda i: m.nvfp4_grouped_gemm_gather(xq_t, sf_t, g_t, qb, sfb, gb, off_d, tok_d, E, 512, Mt,
-                                                          N, K, y=y, workspace=wsp), 4, 5, stream)
+                                                          N, K, y=y, workspace=wsg), 4, 5, stream)
+    ms_ls = time_graph(lambda i: m.nvfp4_grouped_gemm_gather(xq_t, sf_t, g_t, qb, sfb, gb, off_d, tok_d, E, 512, Mt,
+                                                             N, K, y=y, workspace=wsp), 4, 5, stream)
+    del wsg
     gbs = mbytes / (ms * 1e-3) / 1e9
     out["moe_grouped_gather"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
                                  "bytes": mbytes, "tokens_quantised": 512, "routed_rows": Mt,
-                                 "tflops": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12}
+                                 "tflops": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12,
+                                 "rows": "copied out by the preparation kernel",
+                                 "us_load_stage_gather4": ms_ls * 1e3}
     # the same weights read as interleaved gate/up rows, SwiGLU fused into the epilogue
     y_act = torch.empty((Mt, N // 2), dtype=torch.bfloat16, device=dev)
     ms = time_graph(lambda i: m.nvfp4_grouped_gemm_swiglu(qa, sfa, ga, qb, sfb, gb, off_d, E, Mt, N, K,

@@ -157,10 +157,16 @@ int nvfp4_grouped_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, co
  *                    reported as NVFP4_ERR_BAD_OFFSETS in *dev_status (its row's output is
  *                    then unspecified; nothing is read out of bounds)
  *   y                bf16 [M_total, N], routed-row order
- * Other arguments and the workspace as nvfp4_grouped_gemm. Rows are fetched with TMA
- * tile::gather4 (four token rows per instruction); the result equals nvfp4_grouped_gemm
+ *   workspace        nvfp4_grouped_gemm_gather_workspace_bytes(E, M_total, N, K) bytes: the
+ *                    preparation kernel then copies the routed rows out (M_total x K/2 bytes,
+ *                    a few microseconds) and the GEMM reads them as plain tiles (fastest).
+ *                    With only nvfp4_grouped_gemm_workspace_bytes(E, M_total, N, K) bytes the
+ *                    GEMM's load stage fetches the rows itself with TMA tile::gather4 (four
+ *                    token rows per instruction; no copy, more issue work per stage).
+ * Other arguments as nvfp4_grouped_gemm. Either way the result equals nvfp4_grouped_gemm
  * on the gathered rows bit for bit.
  */
+size_t nvfp4_grouped_gemm_gather_workspace_bytes(int32_t E, int64_t M_total, int64_t N, int64_t K);
 int nvfp4_grouped_gemm_gather(const uint8_t* a_tok, const uint8_t* sfa_tok, const float* ga, const uint8_t* b,
                               const uint8_t* sfb, const float* gb, const int32_t* expert_offsets,
                               const int32_t* row_token, int32_t E, int64_t T, int64_t M_total, int64_t N, int64_t K,

@@ -35,6 +35,7 @@ STATUS = {0: "NVFP4_OK", -1: "NVFP4_ERR_INVALID_ARG", -2: "NVFP4_ERR_UNSUPPORTED
 EXPORTS = ["nvfp4_status_string", "nvfp4_scale_bytes", "nvfp4_amax_workspace_bytes", "nvfp4_amax",
            "nvfp4_quantize", "nvfp4_gemm_workspace_bytes", "nvfp4_gemm", "nvfp4_gemm_quantize_out",
            "nvfp4_grouped_gemm_workspace_bytes", "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_gather",
+           "nvfp4_grouped_gemm_gather_workspace_bytes",
            "nvfp4_grouped_gemm_swiglu",
            "nvfp4_grouped_gemm_noalloc",
            "nvfp4_encode_e2m1",
@@ -83,6 +84,8 @@ def lib():
             L.nvfp4_grouped_gemm_workspace_bytes.argtypes = [_i32, _i64, _i64, _i64]
             L.nvfp4_grouped_gemm.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64,
                                              _i64, _vp, _vp, _sz, _vp, _vp]
+            L.nvfp4_grouped_gemm_gather_workspace_bytes.restype = _sz
+            L.nvfp4_grouped_gemm_gather_workspace_bytes.argtypes = [_i32, _i64, _i64, _i64]
             L.nvfp4_grouped_gemm_gather.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64,
                                                     _i64, _i64, _vp, _vp, _sz, _vp, _vp]
             L.nvfp4_grouped_gemm_swiglu.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64,
@@ -229,7 +232,9 @@ def nvfp4_grouped_gemm(a, sfa, ga, b, sfb, gb, expert_offsets, E: int, M_total: 
 def nvfp4_grouped_gemm_gather(a_tok, sfa_tok, ga, b, sfb, gb, expert_offsets, row_token, E: int, T: int,
                               M_total: int, N: int, K: int, y=None, workspace=None, dev_status=None, stream=None):
     """Grouped GEMM over routed rows r (sorted by expert) that read token row row_token[r] of
-    the T-row activations a_tok: bf16 [M_total, N] in routed-row order."""
+    the T-row activations a_tok: bf16 [M_total, N] in routed-row order. The default
+    workspace has room for the rows to be copied out ahead of the GEMM; one of
+    nvfp4_grouped_gemm_workspace_bytes bytes makes the GEMM's load stage gather them."""
     for t, n in ((a_tok, "a_tok"), (sfa_tok, "sfa_tok"), (b, "b"), (sfb, "sfb")):
         _cuda(t, torch.uint8, n)
     _cuda(ga, torch.float32, "ga")
@@ -237,7 +242,7 @@ def nvfp4_grouped_gemm_gather(a_tok, sfa_tok, ga, b, sfb, gb, expert_offsets, ro
     _cuda(expert_offsets, torch.int32, "expert_offsets")
     _cuda(row_token, torch.int32, "row_token")
     y = torch.empty((M_total, N), dtype=torch.bfloat16, device=a_tok.device) if y is None else y
-    ws_bytes = nvfp4_grouped_gemm_workspace_bytes(E, M_total, N, K)
+    ws_bytes = nvfp4_grouped_gemm_gather_workspace_bytes(E, M_total, N, K)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=a_tok.device)
     _check("nvfp4_grouped_gemm_gather",
@@ -245,6 +250,10 @@ def nvfp4_grouped_gemm_gather(a_tok, sfa_tok, ga, b, sfb, gb, expert_offsets, ro
                                            _ptr(expert_offsets), _ptr(row_token), E, T, M_total, N, K, _ptr(y),
                                            _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream)))
     return y
+
+
+def nvfp4_grouped_gemm_gather_workspace_bytes(E: int, M_total: int, N: int, K: int) -> int:
+    return int(lib().nvfp4_grouped_gemm_gather_workspace_bytes(E, M_total, N, K))
 
 
 def nvfp4_grouped_gemm_swiglu(a, sfa, ga, b_gu, sfb_gu, gb, expert_offsets, E: int, M_total: int, N_gu: int,

@@ -435,6 +435,17 @@ size_t nvfp4_grouped_gemm_workspace_bytes(int32_t E, int64_t M_total, int64_t N,
   return static_cast<size_t>(grouped_slab_offset(E, M_total) + grouped_max_tiles(E, M_total) * (K / 64) * 512);
 }
 
+// The gather entry's larger workspace: the plain one (rounded up to 256 bytes), then the
+// routed rows copied out of the token activations, [M_total, K/2].
+static size_t gathered_rows_offset(int32_t E, int64_t M_total, int64_t N, int64_t K) {
+  return (nvfp4_grouped_gemm_workspace_bytes(E, M_total, N, K) + 255) / 256 * 256;
+}
+
+size_t nvfp4_grouped_gemm_gather_workspace_bytes(int32_t E, int64_t M_total, int64_t N, int64_t K) {
+  if (E <= 0 || M_total < 0 || K <= 0) return 0;
+  return gathered_rows_offset(E, M_total, N, K) + static_cast<size_t>(M_total) * static_cast<size_t>(K / 2);
+}
+
 // row_token (null: none): routed row r reads row row_token[r] of the T-row activations a.
 static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b, const uint8_t* sfb,
                         const float* gb, const int32_t* expert_offsets, int32_t E, int64_t M_total, int64_t N,
@@ -462,19 +473,28 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   int32_t* n_tiles = reinterpret_cast<int32_t*>(ws);
   int4* tiles = reinterpret_cast<int4*>(ws + 16);
   uint8_t* slabs = ws + grouped_slab_offset(E, M_total);
+  // Token gather: with room for the routed rows the preparation kernel copies them out
+  // (M_total x K/2 bytes, a few microseconds) and the GEMM reads them as plain tiles;
+  // otherwise the GEMM's load stage fetches them four rows per tile::gather4.
+  uint8_t* xg = nullptr;
+  if (row_token && workspace_bytes >= nvfp4_grouped_gemm_gather_workspace_bytes(E, M_total, N, K))
+    xg = ws + gathered_rows_offset(E, M_total, N, K);
   const int64_t words = M_total * (K / 64);
-  int prep_grid = static_cast<int>((words + 255) / 256);
-  if (prep_grid > 4 * d.sms) prep_grid = 4 * d.sms;
+  const int64_t prep_items = xg ? (words > M_total * (K / 32) ? words : M_total * (K / 32)) : words;
+  int prep_grid = static_cast<int>((prep_items + 255) / 256 < 4 * d.sms ? (prep_items + 255) / 256 : 4 * d.sms);
   if (prep_grid < 1) prep_grid = 1;
   rc = from_cuda(launch_grouped_prep(expert_offsets, row_token, static_cast<int>(T), E, static_cast<int>(M_total),
                                      static_cast<int>(K), sfa, n_tiles,
-                                     tiles, slabs, dev_status, prep_grid, st));
+                                     tiles, slabs, dev_status, prep_grid, st, xg ? a : nullptr, xg));
   g_last_launches = 1;
   if (rc) return rc;
 
   CUtensorMap tmW, tmX;
   if ((rc = encode_2d(&tmW, b, static_cast<uint64_t>(E) * N, K / 2, 128))) return rc;
-  if (row_token) {
+  if (xg) {
+    if ((rc = encode_2d(&tmX, xg, M_total, K / 2, 16))) return rc;
+    row_token = nullptr;  // the GEMM reads the copied rows
+  } else if (row_token) {
     if ((rc = encode_2d(&tmX, a, T, K / 2, 1))) return rc;  // one-row boxes for tile::gather4
   } else if ((rc = encode_2d(&tmX, a, M_total, K / 2, 16))) {
     return rc;

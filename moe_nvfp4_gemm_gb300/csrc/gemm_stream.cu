@@ -553,12 +553,15 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
 // Validates expert_offsets, lists the token tiles (<= kGroupTile rows of one
 // expert each; experts without rows get none) and gathers each tile's token
 // scales into its own slab in the 128-row tiled layout, rows starting at 0.
-// Workspace: [0] n_tiles, [16..) int4 tiles[max_tiles], then the slabs.
+// With xg: also copies packed token row row_token[r] of x_tok to row r of xg
+// (the routed rows in expert order), so the GEMM reads them as plain tiles.
+// Workspace: [0] n_tiles, [16..) int4 tiles[max_tiles], then the slabs (then xg).
 __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict__ offsets,
                                                       const int32_t* __restrict__ row_token, int T, int E, int M_total,
                                                       int K, const uint8_t* __restrict__ sfx, int32_t* n_tiles_out,
                                                       int4* __restrict__ tiles, uint8_t* __restrict__ slabs,
-                                                      int32_t* status) {
+                                                      int32_t* status, const uint8_t* __restrict__ x_tok,
+                                                      uint8_t* __restrict__ xg) {
   extern __shared__ int32_t sh[];  // offsets[E+1], tile_base[E+1]
   int32_t* off = sh;
   int32_t* tbase = sh + (E + 1);
@@ -624,6 +627,17 @@ __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict_
                                                           ((src % 128) / 32) * 4);
     *reinterpret_cast<uint32_t*>(slabs + (tile * KC4 + c4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4) = v;
   }
+  if (xg) {
+    // row gather, 16 bytes per thread and step (indices clamped; bad ones are reported above)
+    const int64_t C = K / 32;  // 16-byte chunks per packed row of K / 2 bytes
+    const int64_t chunks = static_cast<int64_t>(M_total) * C;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < chunks; i += (int64_t)gridDim.x * blockDim.x) {
+      const int m = static_cast<int>(i / C);
+      int src = __ldg(row_token + m);
+      src = src < 0 ? 0 : (src >= T ? T - 1 : src);
+      reinterpret_cast<uint4*>(xg)[i] = __ldg(reinterpret_cast<const uint4*>(x_tok) + src * C + (i - m * C));
+    }
+  }
 }
 
 // ---- host launchers -------------------------------------------------------------------
@@ -680,13 +694,14 @@ cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const 
 cudaError_t launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int T, int E, int M_total, int K,
                                 const uint8_t* sfx,
                                 int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
-                                cudaStream_t st) {
+                                cudaStream_t st, const uint8_t* x_tok, uint8_t* xg) {
   const int smem = 2 * (E + 1) * 4;
   if (smem > 48 * 1024) {
     cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_grouped_prep));
     if (e != cudaSuccess) return e;
   }
-  k_grouped_prep<<<grid, 256, smem, st>>>(offsets, row_token, T, E, M_total, K, sfx, n_tiles, tiles, slabs, status);
+  k_grouped_prep<<<grid, 256, smem, st>>>(offsets, row_token, T, E, M_total, K, sfx, n_tiles, tiles, slabs, status,
+                                          x_tok, xg);
   return cudaGetLastError();
 }
 

@@ -65,7 +65,7 @@ cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const 
 cudaError_t launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int T, int E, int M_total, int K,
                                 const uint8_t* sfx,
                                 int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
-                                cudaStream_t st);
+                                cudaStream_t st, const uint8_t* x_tok = nullptr, uint8_t* xg = nullptr);
 int stream_smem_bytes(int stages, int x_rows, int recv_bytes);
 int stream_recv_bytes(int M, int split);
 

@@ -89,6 +89,13 @@ def test_quantize_and_amax_host_validation(lib):
     assert lib.nvfp4_amax(P(8), 100, P(16), P(16), P(16), 4096, None) == -3
 
 
+def test_gather_workspace_holds_the_routed_rows(lib):
+    for E, Mt, N, K in [(256, 4096, 4096, 6144), (3, 17, 128, 64), (1, 1, 8, 64)]:
+        plain = lib.nvfp4_grouped_gemm_workspace_bytes(E, Mt, N, K)
+        assert lib.nvfp4_grouped_gemm_gather_workspace_bytes(E, Mt, N, K) == (plain + 255) // 256 * 256 + Mt * K // 2
+    assert lib.nvfp4_grouped_gemm_gather_workspace_bytes(0, 16, 128, 64) == 0
+
+
 def test_tune_rejects_bad_values(lib):
     assert lib.nvfp4_tune(1, 200) == -1
     assert lib.nvfp4_tune(4, 9) == -1

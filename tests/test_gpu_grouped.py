@@ -206,12 +206,21 @@ def _gathered(qa_tok, sfa_tok, T, K, row_token):
     return qa, sfa
 
 
+def _gather_ws(copy, E, Mt, N, K):
+    """None: the binding's default workspace (rows copied out ahead of the GEMM); else one
+    of the plain grouped size, which makes the GEMM's load stage gather the rows."""
+    if copy:
+        return None
+    return torch.empty(m.nvfp4_grouped_gemm_workspace_bytes(E, Mt, N, K), dtype=torch.uint8, device=dev())
+
+
+@pytest.mark.parametrize("copy", [True, False])
 @pytest.mark.parametrize("T,counts,N,K", [
     (37, (3, 0, 17, 1, 0, 9), 256, 512),
     (200, (64, 65, 1, 70, 0), 136, 1088),
     (5, (40,), 256, 256),                  # more routed rows than tokens: tokens repeat
 ])
-def test_grouped_gather_matches_gathered_plain_and_oracle(T, counts, N, K):
+def test_grouped_gather_matches_gathered_plain_and_oracle(T, counts, N, K, copy):
     rng = np.random.default_rng(T)
     Mt = int(sum(counts))
     row_token = rng.integers(0, T, size=Mt).astype(np.int32)
@@ -221,13 +230,15 @@ def test_grouped_gather_matches_gathered_plain_and_oracle(T, counts, N, K):
     g.qa, g.sfa, g.ga = qa, sfa, ga
     y_plain = g.run()
     y = m.nvfp4_grouped_gemm_gather(to_dev(qa_tok), to_dev(sfa_tok), scalar(ga), to_dev(g.qb), to_dev(g.sfb),
-                                    to_dev(g.gb), to_dev(g.off), to_dev(row_token), g.E, T, Mt, N, K)
+                                    to_dev(g.gb), to_dev(g.off), to_dev(row_token), g.E, T, Mt, N, K,
+                                    workspace=_gather_ws(copy, g.E, Mt, N, K))
     torch.cuda.synchronize()
     assert torch.equal(y, y_plain)
     g.check(y)
 
 
-def test_grouped_gather_moe_workload():
+@pytest.mark.parametrize("copy", [True, False])
+def test_grouped_gather_moe_workload(copy):
     # 512 tokens quantised once, routed top-8 over 256 experts (4096 rows), K = 6144, N = 4096
     T, K, N = 512, 6144, 4096
     tok, _, off = synth.route_topk(T, 256, 8, 1003)
@@ -240,7 +251,7 @@ def test_grouped_gather_moe_workload():
     y_plain = gg.run()
     y = m.nvfp4_grouped_gemm_gather(to_dev(qa_tok), to_dev(sfa_tok), scalar(ga), to_dev(gg.qb), to_dev(gg.sfb),
                                     to_dev(gg.gb), to_dev(gg.off), to_dev(tok.astype(np.int32)), 256, T,
-                                    int(off[-1]), N, K)
+                                    int(off[-1]), N, K, workspace=_gather_ws(copy, 256, int(off[-1]), N, K))
     torch.cuda.synchronize()
     assert torch.equal(y, y_plain)
     rng = np.random.default_rng(5)
@@ -249,13 +260,15 @@ def test_grouped_gather_moe_workload():
     gg.check(y, rows=rows, cols=cols)
 
 
-def test_grouped_gather_bad_token_index_reported():
+@pytest.mark.parametrize("copy", [True, False])
+def test_grouped_gather_bad_token_index_reported(copy):
     T, K, N = 16, 256, 128
     qa_tok, sfa_tok, ga = oracle.quantize(synth.normal_bf16((T, K), 63, 1.0))
     g = Grouped((4, 4), N, K, 64)
     row_token = np.array([0, 1, 2, 3, 4, 5, 16, 7], dtype=np.int32)  # 16 is out of range
     st = torch.zeros(1, dtype=torch.int32, device=dev())
     m.nvfp4_grouped_gemm_gather(to_dev(qa_tok), to_dev(sfa_tok), scalar(ga), to_dev(g.qb), to_dev(g.sfb),
-                                to_dev(g.gb), to_dev(g.off), to_dev(row_token), g.E, T, 8, N, K, dev_status=st)
+                                to_dev(g.gb), to_dev(g.off), to_dev(row_token), g.E, T, 8, N, K, dev_status=st,
+                                workspace=_gather_ws(copy, g.E, 8, N, K))
     torch.cuda.synchronize()
     assert st.item() == -8
