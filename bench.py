@@ -399,31 +399,68 @@ def main():
         return
 
     # ---- end to end through the C ABI with host buffers ------------------------------------
+    # Every step copies its inputs in from pinned host memory and its result out to pinned
+    # host memory. Serial: copy in, GEMM, copy out on one stream. Pipelined (the reported
+    # value): two buffer sets, the copies in on one stream, the GEMMs on the launching
+    # stream, the copies out on a third, so step i's GEMM overlaps step i+1's copy in and
+    # step i-1's copy out, as a caller streaming batches through the GEMM would run it.
     host_in = [t.cpu().pin_memory() for t in sets[0][:6]]
-    host_out = torch.empty((SQ, SQ), dtype=torch.bfloat16).pin_memory()
-    dev_in = [t.clone() for t in sets[0][:6]]
-    y_e2e = torch.empty((SQ, SQ), dtype=torch.bfloat16, device=dev)
-    e2e_steps = max(3, min(args.steps, 20))
+    host_out = [torch.empty((SQ, SQ), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dev_in = [[t.clone() for t in sets[0][:6]] for _ in range(2)]
+    y_e2e = [torch.empty((SQ, SQ), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    e2e_steps = max(4, min(args.steps, 20))
 
-    def e2e_step():
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
-        m.nvfp4_gemm(dev_in[0], dev_in[1], dev_in[2], dev_in[3], dev_in[4], dev_in[5], SQ, SQ, SQ,
-                     y=y_e2e)
-        host_out.copy_(y_e2e, non_blocking=True)
+    def e2e_serial(n):
+        for _ in range(n):
+            for d, h in zip(dev_in[0], host_in):
+                d.copy_(h, non_blocking=True)
+            m.nvfp4_gemm(*dev_in[0], SQ, SQ, SQ, y=y_e2e[0])
+            host_out[0].copy_(y_e2e[0], non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    def e2e_pipelined(n):
+        landed = [torch.cuda.Event() for _ in range(n)]
+        computed = [torch.cuda.Event() for _ in range(n)]
+        copied_out = [torch.cuda.Event() for _ in range(n)]
+        start = torch.cuda.Event()
+        start.record(stream)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(computed[i - 2])  # buffer set b is free again
+                for d, h in zip(dev_in[b], host_in):
+                    d.copy_(h, non_blocking=True)
+                landed[i].record(s_in)
+            stream.wait_event(landed[i])
+            if i >= 2:
+                stream.wait_event(copied_out[i - 2])  # y[b] has left the device
+            m.nvfp4_gemm(*dev_in[b], SQ, SQ, SQ, y=y_e2e[b], stream=stream)
+            computed[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(computed[i])
+                host_out[b].copy_(y_e2e[b], non_blocking=True)
+                copied_out[i].record(s_out)
+        stream.wait_event(copied_out[n - 1])
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+
+    def timed_e2e(fn):
+        fn(2)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn(e2e_steps)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return reduce_max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+
+    e2e_serial_ms = timed_e2e(e2e_serial)
+    e2e_ms = timed_e2e(e2e_pipelined)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size()
 
     # ---- breakdown of the other workloads ---------------------------------------------------
     breakdown = {}
@@ -445,7 +482,9 @@ def main():
                      "kernel": "k_gemm_dense_pair",
                      "peak_source": f"{peaks['source']} bf16 {peaks['bf16']:.0f} TFLOP/s x {FP4_OVER_BF16:g} (nominal fp4/bf16)"},
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "pipeline": "2 buffer sets; copies in, GEMMs and copies out on three streams",
+                "serial_value": flops / (e2e_serial_ms * 1e-3) / 1e12},
         "gpu_launches": launches,
         "clocks": clocks,
         "breakdown": breakdown,
