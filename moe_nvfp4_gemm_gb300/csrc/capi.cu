@@ -479,9 +479,9 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   uint8_t* xg = nullptr;
   if (row_token && workspace_bytes >= nvfp4_grouped_gemm_gather_workspace_bytes(E, M_total, N, K))
     xg = ws + gathered_rows_offset(E, M_total, N, K);
-  const int64_t words = M_total * (K / 64);
-  const int64_t prep_items = xg ? (words > M_total * (K / 32) ? words : M_total * (K / 32)) : words;
-  int prep_grid = static_cast<int>((prep_items + 255) / 256 < 4 * d.sms ? (prep_items + 255) / 256 : 4 * d.sms);
+  // one warp per routed row and step (eight per block)
+  const int64_t prep_blocks = (M_total + 7) / 8;
+  int prep_grid = static_cast<int>(prep_blocks < 4 * d.sms ? prep_blocks : 4 * d.sms);
   if (prep_grid < 1) prep_grid = 1;
   rc = from_cuda(launch_grouped_prep(expert_offsets, row_token, static_cast<int>(T), E, static_cast<int>(M_total),
                                      static_cast<int>(K), sfa, n_tiles,

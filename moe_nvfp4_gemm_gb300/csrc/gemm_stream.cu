@@ -583,13 +583,31 @@ __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict_
     }
     return;
   }
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int e = 0; e < E; ++e) {
+  {
+    // tile bases: an exclusive scan of the experts' tile counts, each thread summing a
+    // contiguous run of experts, the runs combined across the block
+    __shared__ int warp_sum[8];
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int e0 = min(E, static_cast<int>(threadIdx.x) * per), e1 = min(E, e0 + per);
+    int mine = 0;
+    for (int e = e0; e < e1; ++e) mine += (off[e + 1] - off[e] + kGroupTile - 1) / kGroupTile;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = mine;  // inclusive scan within the warp
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    if (lane == 31) warp_sum[wid] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < wid; ++w) before += warp_sum[w];
+    int acc = before + incl - mine;
+    for (int e = e0; e < e1; ++e) {
       tbase[e] = acc;
       acc += (off[e + 1] - off[e] + kGroupTile - 1) / kGroupTile;
     }
-    tbase[E] = acc;
+    if (threadIdx.x == blockDim.x - 1) tbase[E] = before + incl;
   }
   __syncthreads();
   if (blockIdx.x == 0) {
@@ -600,12 +618,15 @@ __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict_
     }
     if (threadIdx.x == 0) *n_tiles_out = tbase[E];
   }
-  // scale gather: one 4-byte word = (row m, four consecutive 16-element blocks)
+  // One warp per routed row m at a time: its expert (binary search over the offsets), its
+  // tile and row within the tile, and its source row; then the lanes gather the row's
+  // scale words (one 4-byte word = four consecutive 16-element blocks) into the tile's
+  // slab and, with xg, copy its packed row 16 bytes per lane and step.
   const int64_t KC4 = K / 64;
-  const int64_t words = static_cast<int64_t>(M_total) * KC4;
-  for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < words; w += (int64_t)gridDim.x * blockDim.x) {
-    const int m = static_cast<int>(w / KC4);
-    const int c4 = static_cast<int>(w % KC4);
+  const int64_t C = K / 32;  // 16-byte chunks per packed row of K / 2 bytes
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int m = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); m < M_total; m += warps) {
     int lo = 0, hi = E;  // expert e with off[e] <= m < off[e+1]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -613,29 +634,24 @@ __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict_
     }
     while (off[lo + 1] <= m) ++lo;  // skip empty experts sharing the same offset
     const int j = m - off[lo];
-    const int tile = tbase[lo] + j / kGroupTile;
+    const int64_t tile = tbase[lo] + j / kGroupTile;
     const int r = j % kGroupTile;
     int src = m;  // the row of x (and of its scales) this routed row reads
     if (row_token) {
       src = __ldg(row_token + m);
       if (src < 0 || src >= T) {  // reported, and clamped so that nothing is read out of bounds
-        if (c4 == 0) report_status(status, kStatusBadOffsets);
+        if (lane == 0) report_status(status, kStatusBadOffsets);
         src = src < 0 ? 0 : T - 1;
       }
     }
-    const uint32_t v = *reinterpret_cast<const uint32_t*>(sfx + ((src / 128) * KC4 + c4) * 512 + (src % 32) * 16 +
-                                                          ((src % 128) / 32) * 4);
-    *reinterpret_cast<uint32_t*>(slabs + (tile * KC4 + c4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4) = v;
-  }
-  if (xg) {
-    // row gather, 16 bytes per thread and step (indices clamped; bad ones are reported above)
-    const int64_t C = K / 32;  // 16-byte chunks per packed row of K / 2 bytes
-    const int64_t chunks = static_cast<int64_t>(M_total) * C;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < chunks; i += (int64_t)gridDim.x * blockDim.x) {
-      const int m = static_cast<int>(i / C);
-      int src = __ldg(row_token + m);
-      src = src < 0 ? 0 : (src >= T ? T - 1 : src);
-      reinterpret_cast<uint4*>(xg)[i] = __ldg(reinterpret_cast<const uint4*>(x_tok) + src * C + (i - m * C));
+    const uint8_t* sfx_row = sfx + (static_cast<int64_t>(src / 128) * KC4) * 512 + (src % 32) * 16 + ((src % 128) / 32) * 4;
+    uint8_t* slab_row = slabs + tile * KC4 * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4;
+    for (int64_t c4 = lane; c4 < KC4; c4 += 32)
+      *reinterpret_cast<uint32_t*>(slab_row + c4 * 512) = *reinterpret_cast<const uint32_t*>(sfx_row + c4 * 512);
+    if (xg) {
+      const uint4* from = reinterpret_cast<const uint4*>(x_tok) + static_cast<int64_t>(src) * C;
+      uint4* to = reinterpret_cast<uint4*>(xg) + static_cast<int64_t>(m) * C;
+      for (int64_t ch = lane; ch < C; ch += 32) to[ch] = __ldg(from + ch);
     }
   }
 }

@@ -87,6 +87,15 @@ def test_grouped_ragged_counts(counts):
     g.check(g.run())
 
 
+def test_grouped_many_experts():
+    # more experts than the preparation kernel has threads: each thread scans a run of
+    # experts' tile counts (empty experts among them)
+    rng = np.random.default_rng(25)
+    counts = tuple(int(c) for c in rng.integers(0, 4, size=600))
+    g = Grouped(counts, 128, 256, 25)
+    g.check(g.run())
+
+
 def test_grouped_ragged_n_and_k():
     g = Grouped((10, 40, 0, 7), 136, 1088, 22)
     g.check(g.run())
