@@ -123,3 +123,19 @@ def test_global_scale_makes_tensor_max_land_on_448_times_six():
     q, sf, g = oracle.quantize(x)
     s = oracle.sf_unswizzle(sf, 128, 256)
     assert s.max() == 0x7E  # the block holding the tensor's amax gets scale 448
+
+
+def test_row_gather_commutes_with_quantisation():
+    # Blocks run along K, so quantising gathered rows (with the same global scale) gives
+    # exactly the gathered codes and scales of the quantised tensor; the routed-row path
+    # (tokens quantised once, rows gathered by token) depends on this.
+    T, K = 40, 320
+    x = synth.normal_bf16((T, K), 71, 1.0, 1e-2)
+    g = oracle.global_scale(oracle.amax(x))
+    rows = np.random.default_rng(72).integers(0, T, size=97)  # repeats and omissions
+    q_all, sf_all, _ = oracle.quantize(x, g)
+    q_sel, sf_sel, _ = oracle.quantize(np.ascontiguousarray(x[rows]), g)
+    assert np.array_equal(q_sel, q_all[rows])
+    lin_all = oracle.sf_unswizzle(sf_all, T, K)
+    lin_sel = oracle.sf_unswizzle(sf_sel, len(rows), K)
+    assert np.array_equal(lin_sel, lin_all[rows])
