@@ -30,7 +30,8 @@
  *     (NVFP4_ERR_CUDA). Errors found on the device (malformed expert offsets, a
  *     wait that timed out) are written to *dev_status when dev_status is not
  *     NULL; the caller zeroes it beforehand and reads it after synchronising.
- *   - Shapes: K % 64 == 0, N % 8 == 0, M >= 0, all sizes < 2^31. Data, scale and
+ *   - Shapes: K % 64 == 0, N % 8 == 0, M >= 0, all sizes < 2^31 (grouped calls: at
+ *     most 2^30 routed rows, E <= 16384 experts, E * N < 2^31). Data, scale and
  *     output base pointers are 16-byte aligned (TMA). M == 0 is a no-op.
  *   - The device must be compute capability 10.3 (GB300, sm_103a).
  */

@@ -457,6 +457,9 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   int rc = check_gemm_shape(M_total, N, K);
   if (rc) return rc;
   if (static_cast<int64_t>(E) * N > kMaxDim || E > 16384) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  // routed rows are indexed with 32-bit integers on the device, with headroom for the
+  // preparation kernel's grid stride
+  if (M_total > (int64_t(1) << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (M_total == 0) return NVFP4_OK;
   if (!a || !sfa || !ga || !b || !sfb || !gb || !expert_offsets || !y) return NVFP4_ERR_INVALID_ARG;
   if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(y))

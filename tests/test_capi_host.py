@@ -77,6 +77,7 @@ def test_grouped_host_validation(lib):
     assert g(4, 100, 256, need - 1) == -6               # short workspace
     assert g(4, 100, 272, need) == -3                   # workspace not 256-byte aligned
     assert g(4, 100, 256, need, off=0) == -1            # null offsets
+    assert g(4, (1 << 30) + 1, 256, 1 << 62) == -2      # more routed rows than 32-bit indexing allows
 
 
 def test_quantize_and_amax_host_validation(lib):
