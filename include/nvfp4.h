@@ -188,7 +188,8 @@ int nvfp4_grouped_gemm_gather(const uint8_t* a_tok, const uint8_t* sfa_tok, cons
  *   workspace        nvfp4_grouped_gemm_workspace_bytes(E, M_total, N_gu, K) bytes
  * The activation runs in fp32 on g_a * g_b * accumulator values before the one bf16
  * rounding of the product; the result agrees with the oracle within the bound the
- * GEMM tolerance of each factor implies (1.1 t_g (|u| + t_u) + |silu(g)| t_u + 2^-8 |y|).
+ * GEMM tolerance of each factor implies:
+ * (1 + 2^-8) (1.1 t_g (|u| + t_u) + |silu(g)| t_u) + 2^-8 |y|.
  */
 int nvfp4_grouped_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b_gu,
                               const uint8_t* sfb_gu, const float* gb, const int32_t* expert_offsets, int32_t E,

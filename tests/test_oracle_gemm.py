@@ -267,16 +267,72 @@ def test_swiglu_oracle_is_interleaved_grouped_gemm_then_silu_times_up():
     assert np.array_equal(ys, y[:, cols])
 
 
-def test_swiglu_tolerance_bound_edges():
-    gate = np.array([2.0, -3.0, 0.0, 10.0])
-    up = np.array([1.5, 0.25, 4.0, -2.0])
-    adg = np.array([50.0, 10.0, 100.0, 5.0])
-    adu = np.array([20.0, 30.0, 1.0, 7.0])
+def _bf16_round(v):
+    """float64 -> nearest bf16 value (ties to even), through float32 as the GPU does."""
+    b = np.asarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16 << 16
+    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def _worst_gpu_outputs(gate, up, adg, adu, rel=4e-3, absk=1e-5):
+    """Outputs a GPU within the GEMM tolerance could return: gate and up moved to every
+    corner of their tolerance boxes (shrunk by 2^-20 so that float32 stays inside), the
+    activation in float32, then either the bf16 rounding or a worst-case 2^-9 relative
+    error pushed away from the exact product."""
+    tg = rel * np.abs(gate) + absk * adg
+    tu = rel * np.abs(up) + absk * adu
     y = oracle.silu(gate) * up
-    tg = 4e-3 * np.abs(gate) + 1e-5 * adg
-    tu = 4e-3 * np.abs(up) + 1e-5 * adu
-    bound = 1.1 * tg * (np.abs(up) + tu) + np.abs(oracle.silu(gate)) * tu + 2.0 ** -8 * np.abs(y)
-    ok, worst = oracle.within_tolerance_swiglu(y + 0.999 * bound, gate, up, adg, adu)
-    assert ok and worst < 1.0
-    ok, worst = oracle.within_tolerance_swiglu(y - 1.001 * bound, gate, up, adg, adu)
-    assert not ok and worst > 1.0
+    outs = []
+    for sg in (-1.0, 1.0):
+        for su in (-1.0, 1.0):
+            g1 = np.float32(gate + sg * tg * (1 - 2.0 ** -20))
+            u1 = np.float32(up + su * tu * (1 - 2.0 ** -20))
+            act = np.float32(g1 / (np.float32(1) + np.float32(np.exp(-g1.astype(np.float64)))))
+            prod = (act * u1).astype(np.float64)
+            outs.append(_bf16_round(prod))
+            away = np.sign(prod - y)
+            outs.append(prod * (1 + away * np.sign(prod) * 2.0 ** -9))
+    return outs
+
+
+def test_silu_lipschitz_constant_below_1_1():
+    # silu'(v) = s(v) (1 + v (1 - s(v))), s the logistic function: its maximum (at v ~ 2.3994)
+    # is the Lipschitz constant the SwiGLU tolerance takes as 1.1
+    special = pytest.importorskip("scipy.special")
+    v = np.linspace(-60.0, 60.0, 1_200_001)
+    s = special.expit(v)
+    d = s * (1 + v * (1 - s))
+    assert 1.0997 < d.max() < 1.1 and abs(v[d.argmax()] - 2.3994) < 1e-3
+    assert d.min() > -0.1  # the steepest descent (near v = -2.4) is far smaller in magnitude
+    # the oracle's silu has that derivative (central differences)
+    h = 1e-6
+    fd = (oracle.silu(v[::997] + h) - oracle.silu(v[::997] - h)) / (2 * h)
+    assert np.allclose(fd, d[::997], atol=1e-8)
+
+
+def test_swiglu_tolerance_holds_for_every_output_within_the_gemm_bounds():
+    # soundness: any gate/up within their GEMM tolerances, activated in fp32 and rounded to
+    # bf16 (or off by a full 2^-9 the other way), passes the propagated bound
+    rng = np.random.default_rng(7)
+    n = 200_000
+    gate = rng.normal(0, 3, n) * rng.choice([1e-3, 1, 4], n)
+    up = rng.normal(0, 3, n) * rng.choice([1e-3, 1, 4], n)
+    adg = np.abs(rng.normal(0, 1, n)) * rng.choice([0, 10, 1e3, 5e4], n)
+    adu = np.abs(rng.normal(0, 1, n)) * rng.choice([0, 10, 1e3, 5e4], n)
+    for y in _worst_gpu_outputs(gate, up, adg, adu):
+        ok, worst = oracle.within_tolerance_swiglu(y, gate, up, adg, adu)
+        assert ok, worst
+
+
+@pytest.mark.parametrize("gate,up,adg,adu,term", [
+    (2.15, 1.0, 49_000.0, 0.0, "slope of silu times |u|"),   # g' spans the steepest stretch
+    (5.0, 0.1, 0.0, 49_960.0, "|silu(g)| times t_u"),
+    (1.9, 0.0, 99_240.0, 1e5, "slope times t_g t_u"),           # y = 0: all error from both bounds
+])
+def test_swiglu_tolerance_is_tight(gate, up, adg, adu, term):
+    # in each regime one part of the bound dominates and a GPU result at a corner of the
+    # tolerance boxes uses at least 95 % of it, so dropping or shrinking that part (or the
+    # Lipschitz constant) makes these corner outputs fail the check above
+    g, u, ag, au = (np.array([v]) for v in (gate, up, adg, adu))
+    ratios = [oracle.within_tolerance_swiglu(y, g, u, ag, au)[1] for y in _worst_gpu_outputs(g, u, ag, au)]
+    assert 0.95 <= max(ratios) <= 1.0, (term, ratios)
