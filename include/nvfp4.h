@@ -199,9 +199,9 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, const float*
 /*
  * Allocation-free variant of nvfp4_grouped_gemm. The pages have no counterpart;
  * it exists for callers that cannot call cudaMalloc at the point where they run
- * the MoE layer: code that runs while a stream is being captured into a CUDA
- * graph, runtimes that give kernels a fixed memory budget and no allocator, and
- * plugins that must not reach into the host program's allocator.
+ * the MoE layer: runtimes that hand kernels a fixed memory budget and offer no
+ * allocator, and plugins or extensions that must not reach into the host
+ * program's allocator (whose pools and bookkeeping they do not own).
  *
  * Same arguments and result as nvfp4_grouped_gemm, minus the workspace: the
  * scratch (tile list and per-tile activation scales) lives in one array of
@@ -211,8 +211,12 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, const float*
  *     M_total, N, K) exceeds NVFP4_NOALLOC_SCRATCH_BYTES (256 experts with 4096
  *     routed rows and K = 6144 need 15.0 MiB and fit).
  *   - The first call on a device looks up the array's device address with that
- *     device current (cudaGetSymbolAddress); make that first call before any
- *     stream capture. Later calls do no CUDA call besides the launches.
+ *     device current (cudaGetSymbolAddress) and caches it; make that first call
+ *     before any stream capture. Every call also makes the CUDA runtime calls
+ *     nvfp4_grouped_gemm makes: cudaGetDevice, cudaGetLastError after each
+ *     launch, the device-attribute queries of the first call on a device, and
+ *     cudaFuncSetAttribute (maximum dynamic shared memory) at the first launch
+ *     of each kernel variant on a device; none of them allocates.
  *   - Every call on a device shares the one array, which keeps the last call's
  *     contents. The kernels write every scratch byte they read, so nothing needs
  *     clearing between calls, but calls that overlap on the GPU (unordered streams)
