@@ -34,6 +34,9 @@ SQ = 8192
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense ratio (fp4 13.5 PF vs bf16 2.25 PF)
+NOMINAL_FP4_TFLOPS = 13500.0  # GB300 dense FP4, vendor figure
+NOMINAL_HBM_GBS = 8000.0      # ~8 TB/s HBM3e
+MIN_CLOCK_SAMPLES = 20        # a median clock from fewer samples is flagged
 
 
 def parse():
@@ -44,7 +47,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-breakdown", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--only", choices=["square", "decode", "moe", "prefill"], default=None,
+    ap.add_argument("--sustained-seconds", type=float, default=3.0)
+    ap.add_argument("--only", choices=["square", "decode", "moe", "prefill", "tiny"], default=None,
                     help="run only this breakdown workload (for profiling) and print its numbers")
     return ap.parse_args()
 
@@ -116,6 +120,7 @@ class NvmlSampler:
         fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
         self.reasons_fn = fn if fn is not None else self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
         self.samples, self.reason_bits, self.stop_flag, self.thread = [], 0, False, None
+        self.period_s = 0.0002
 
     def _run(self):
         ct = self.ct
@@ -125,7 +130,7 @@ class NvmlSampler:
                 self.samples.append(mhz.value)
             if self.reasons_fn(self.h, ct.byref(bits)) == 0:
                 self.reason_bits |= bits.value
-            time.sleep(0.002)
+            time.sleep(self.period_s)
 
     def start(self):
         self.thread = self.threading.Thread(target=self._run, daemon=True)
@@ -137,9 +142,10 @@ class NvmlSampler:
         smax = self.ct.c_uint()
         self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, self.ct.byref(smax))
         reasons = sorted(n for b, n in self.REASONS.items() if self.reason_bits & b)
+        n = len(self.samples)
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": smax.value or None, "reasons": reasons, "samples": len(self.samples),
-                "source": "nvml, 2 ms"}
+                "sm_max_mhz": smax.value or None, "reasons": reasons, "samples": n,
+                "sampler": f"nvml, every {self.period_s * 1e3:g} ms", "few_samples": n < MIN_CLOCK_SAMPLES}
 
 
 def clock_sampler(torch_device, index):
@@ -173,7 +179,8 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0, "sampler": "none", "few_samples": True}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -199,7 +206,8 @@ class ClockSampler:
         busy = [s for s in sm if s > 0]
         return {"sm_mhz": statistics.median(busy) if busy else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "sampler": "nvidia-smi, every 100 ms",
+                "few_samples": len(sm) < MIN_CLOCK_SAMPLES}
 
 
 # Sources each profiled kernel is built from: a recorded DRAM traffic figure stays valid
@@ -462,6 +470,10 @@ def main():
     e2e_ms = timed_e2e(e2e_pipelined)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = host_out[0].numel() * host_out[0].element_size()
+    sustained = None
+    if args.sustained_seconds > 0 and not args.no_breakdown:
+        sustained = run_sustained(m, dev, stream, gemm, peaks["bf16_sustained"] * FP4_OVER_BF16,
+                                  args.sustained_seconds, local)
 
     # ---- breakdown of the other workloads ---------------------------------------------------
     breakdown = {}
@@ -481,7 +493,9 @@ def main():
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
                      "frac": achieved / fp4_peak, "traffic": profiled_traffic("k_gemm_dense_pair"),
                      "kernel": "k_gemm_dense_pair",
-                     "peak_source": f"{peaks['source']} bf16 {peaks['bf16']:.0f} TFLOP/s x {FP4_OVER_BF16:g} (nominal fp4/bf16)"},
+                     "peak_source": f"{peaks['source']} bf16 {peaks['bf16']:.0f} TFLOP/s x {FP4_OVER_BF16:g} (nominal fp4/bf16)",
+                     "frac_vs_nominal_13p5PF": achieved / NOMINAL_FP4_TFLOPS},
+        "sustained": sustained,
         "e2e": {"value": flops / (e2e_serial_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_serial_ms,
                 "pipelined_value": flops / (e2e_ms * 1e-3) / 1e12,
@@ -493,6 +507,8 @@ def main():
     if rank == 0 and world == 1 or rank == 0:
         try:
             line["cpu_baseline"] = cpu_oracle_gemm_rate(args.cpu_seconds) if world == 1 else None
+            if line["cpu_baseline"] is not None:
+                line["cpu_baseline"]["tiny"] = cpu_oracle_tiny()
         except Exception as ex:  # the baseline is reported, never required
             line["cpu_baseline"] = {"error": str(ex)}
         print(json.dumps(line), flush=True)
@@ -553,6 +569,8 @@ def run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak, 
         run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out)
     if only in (None, "prefill"):
         run_prefill(m, synth, dev, stream, to_dev, quantize_dev, hbm, fp4_peak, out)
+    if only in (None, "tiny"):
+        run_tiny(m, synth, dev, stream, to_dev, quantize_dev, out)
     return out
 
 
@@ -579,6 +597,7 @@ def run_decode(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
         gbs = wbytes / (ms * 1e-3) / 1e9
         gbs_pdl = wbytes / (ms_pdl * 1e-3) / 1e9
         out[f"decode_M{M}"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm,
+                               "hbm_frac_vs_8TBps": gbs / NOMINAL_HBM_GBS,
                                "bytes": wbytes, "timing": "CUDA graph of 16 calls over 8 weight copies",
                                "us_eager_per_launch_events": ms_eager * 1e3,
                                "us_pdl": ms_pdl * 1e3, "weight_GBps_pdl": gbs_pdl,
@@ -637,6 +656,7 @@ def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
     mbytes = hit * (N * K // 2 + sfb_bytes)
     gbs = mbytes / (ms * 1e-3) / 1e9
     out["moe_grouped"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
+                          "hbm_frac_vs_8TBps": gbs / NOMINAL_HBM_GBS,
                           "bytes": mbytes, "tflops": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12}
     # the same tokens quantised once (512 rows) and gathered by routed row: copied out by the
     # preparation kernel (default workspace), or fetched by the GEMM's load stage (plain-size
@@ -673,6 +693,7 @@ def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
     mbytes = hit * (N * K // 2 + sfb_bytes)
     gbs = mbytes / (ms * 1e-3) / 1e9
     out["moe_grouped_skewed"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
+                                 "hbm_frac_vs_8TBps": gbs / NOMINAL_HBM_GBS,
                                  "max_rows_per_expert": int(np.diff(off_s).max()), "routing": "Zipf(1) popularity",
                                  "bytes": mbytes, "tflops": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12}
     del qb, sfb, wsp
@@ -681,27 +702,37 @@ def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
 
 def run_prefill(m, synth, dev, stream, to_dev, quantize_dev, hbm, fp4_peak, out):
     import torch
-    # prefill: quantize x (4096 x 8192) on the GPU, GEMM against pre-quantised W (28672 x 8192)
+    # prefill: quantize x (4096 x 8192) on the GPU, GEMM against pre-quantised W (28672 x 8192).
+    # The quantiser and amax read their input from HBM: 4 rotating activation buffers
+    # (4 x 67 MB in, 4 x 19 MB out: 344 MB > the 129 MB L2), so no call finds its input in L2.
     Mp, Np, Kp = 4096, 28672, 8192
-    x = to_dev(synth.normal_bf16((Mp, Kp), 2 * 4, 1.0, 1e-3))
+    RQ = 4
+    x0 = to_dev(synth.normal_bf16((Mp, Kp), 2 * 4, 1.0, 1e-3))
+    xs = [x0] + [x0.clone() for _ in range(RQ - 1)]
     wq, sfw, gw = quantize_dev(to_dev(synth.normal_bf16((Np, Kp), 2 * 4 + 1, 0.02)))
     wcopies = [(wq, sfw), (wq.clone(), sfw.clone())]
     amax = torch.empty(1, dtype=torch.float32, device=dev)
     g = torch.empty(1, dtype=torch.float32, device=dev)
-    q = torch.empty((Mp, Kp // 2), dtype=torch.uint8, device=dev)
-    sf = torch.empty(m.nvfp4_scale_bytes(Mp, Kp), dtype=torch.uint8, device=dev)
+    qs = [torch.empty((Mp, Kp // 2), dtype=torch.uint8, device=dev) for _ in range(RQ)]
+    sfs = [torch.empty(m.nvfp4_scale_bytes(Mp, Kp), dtype=torch.uint8, device=dev) for _ in range(RQ)]
+    q, sf = qs[0], sfs[0]
     aws = torch.empty(m.nvfp4_amax_workspace_bytes(Mp * Kp), dtype=torch.uint8, device=dev)
     yp = torch.empty((Mp, Np), dtype=torch.bfloat16, device=dev)
-    m.nvfp4_amax(x, amax, g, aws)
-    ms_q = time_graph(lambda i: m.nvfp4_quantize(x, g, q, sf), 10, 10, stream)
-    ms_amax = time_graph(lambda i: m.nvfp4_amax(x, amax, g, aws), 10, 10, stream)
+    m.nvfp4_amax(x0, amax, g, aws)
+    ms_q = time_graph(lambda i: m.nvfp4_quantize(xs[i % RQ], g, qs[i % RQ], sfs[i % RQ]), 12, 10, stream)
+    ms_amax = time_graph(lambda i: m.nvfp4_amax(xs[i % RQ], amax, g, aws), 12, 10, stream)
+    # the same calls repeated on one buffer (input resident in L2), for comparison
+    ms_q_l2 = time_graph(lambda i: m.nvfp4_quantize(x0, g, q, sf), 10, 10, stream)
+    ms_amax_l2 = time_graph(lambda i: m.nvfp4_amax(x0, amax, g, aws), 10, 10, stream)
+    m.nvfp4_quantize(x0, g, q, sf)
     ms_g = time_launches(lambda i: m.nvfp4_gemm(q, sf, g, wcopies[i % 2][0], wcopies[i % 2][1], gw,
                                                 Mp, Np, Kp, y=yp), 20, stream)
 
     def together(i):
+        x, qq, ss = xs[i % RQ], qs[i % RQ], sfs[i % RQ]
         m.nvfp4_amax(x, amax, g, aws)
-        m.nvfp4_quantize(x, g, q, sf)
-        m.nvfp4_gemm(q, sf, g, wcopies[i % 2][0], wcopies[i % 2][1], gw, Mp, Np, Kp, y=yp)
+        m.nvfp4_quantize(x, g, qq, ss)
+        m.nvfp4_gemm(qq, ss, g, wcopies[i % 2][0], wcopies[i % 2][1], gw, Mp, Np, Kp, y=yp)
 
     ms_t = time_launches(together, 20, stream)
     # layer chain: the GEMM's output as the next layer's NVFP4 input, with a given global
@@ -718,15 +749,88 @@ def run_prefill(m, synth, dev, stream, to_dev, quantize_dev, hbm, fp4_peak, out)
 
     ms_gtq = time_launches(gemm_then_quantize, 20, stream)
     qbytes = Mp * Kp * 2 + Mp * Kp // 2 + m.nvfp4_scale_bytes(Mp, Kp)
+    abytes = Mp * Kp * 2
+    gemm_tf = 2.0 * Mp * Np * Kp / (ms_g * 1e-3) / 1e12
     out["prefill"] = {
         "quantize_us": ms_q * 1e3, "quantize_GBps": qbytes / (ms_q * 1e-3) / 1e9,
-        "quantize_hbm_frac": qbytes / (ms_q * 1e-3) / 1e9 / hbm, "quantize_bytes": qbytes,
-        "amax_us": ms_amax * 1e3, "amax_GBps": Mp * Kp * 2 / (ms_amax * 1e-3) / 1e9,
-        "gemm_us": ms_g * 1e3, "gemm_tflops": 2.0 * Mp * Np * Kp / (ms_g * 1e-3) / 1e12,
-        "gemm_frac": 2.0 * Mp * Np * Kp / (ms_g * 1e-3) / 1e12 / fp4_peak,
+        "quantize_hbm_frac": qbytes / (ms_q * 1e-3) / 1e9 / hbm,
+        "quantize_hbm_frac_vs_8TBps": qbytes / (ms_q * 1e-3) / 1e9 / NOMINAL_HBM_GBS, "quantize_bytes": qbytes,
+        "amax_us": ms_amax * 1e3, "amax_GBps": abytes / (ms_amax * 1e-3) / 1e9,
+        "amax_hbm_frac": abytes / (ms_amax * 1e-3) / 1e9 / hbm,
+        "quantize_amax_input": f"from HBM: {RQ} rotating activation buffers ({RQ * (qbytes) / 1e6:.0f} MB)",
+        "quantize_us_input_in_l2": ms_q_l2 * 1e3, "amax_us_input_in_l2": ms_amax_l2 * 1e3,
+        "gemm_us": ms_g * 1e3, "gemm_tflops": gemm_tf, "gemm_frac": gemm_tf / fp4_peak,
+        "gemm_frac_vs_nominal_13p5PF": gemm_tf / NOMINAL_FP4_TFLOPS,
         "together_us": ms_t * 1e3,
+        "together": "amax + quantize (rotating activations) + GEMM, per step",
         "gemm_nvfp4_out_us": ms_gq * 1e3, "gemm_nvfp4_out_tflops": 2.0 * Mp * Np * Kp / (ms_gq * 1e-3) / 1e12,
         "gemm_then_quantize_us": ms_gtq * 1e3}
+
+
+def run_tiny(m, synth, dev, stream, to_dev, quantize_dev, out):
+    """The tiny workload (128 x 128 x 256, x and W ~ N(0,1), seed 0) on the GPU: both
+    operands quantised by nvfp4_quantize, then the GEMM; per-launch event times. Its
+    parity is a test case; the oracle's time for it is reported with the CPU baseline."""
+    import torch
+    M, N, K = 128, 128, 256
+    xb, wb = synth.dense_inputs(M, N, K, 0)
+    xd, wd = to_dev(xb), to_dev(wb)
+    ms_q = time_launches(lambda i: quantize_dev(xd), 50, stream)
+    xa, sa, g1 = quantize_dev(xd)
+    wa, sw, g2 = quantize_dev(wd)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ms = time_launches(lambda i: m.nvfp4_gemm(xa, sa, g1, wa, sw, g2, M, N, K, y=y), 50, stream)
+    out["tiny"] = {"gpu_gemm_us": ms * 1e3, "gpu_amax_quantize_us": ms_q * 1e3,
+                   "note": "128 x 128 x 256; per-launch CUDA events; oracle ms in cpu_baseline.tiny"}
+
+
+def cpu_oracle_tiny():
+    """The oracle on the tiny workload, in ms: quantising x and W, and the float64 GEMM."""
+    import oracle
+    import synth
+    M, N, K = 128, 128, 256
+    xb, wb = synth.dense_inputs(M, N, K, 0)
+    reps = 20
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        qa, sfa, ga = oracle.quantize(xb)
+        qb, sfb, gb = oracle.quantize(wb)
+    tq = (time.perf_counter() - t0) / reps
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.gemm(qa, sfa, ga, qb, sfb, gb, M, N, K)
+    tg = (time.perf_counter() - t0) / reps
+    return {"oracle_gemm_ms": tg * 1e3, "oracle_quantize_x_and_w_ms": tq * 1e3, "cores": oracle.num_threads(),
+            "workload": "tiny 128 x 128 x 256, seed 0 (float64 on the host cores)"}
+
+
+def run_sustained(m, dev, stream, gemm, fp4_peak_sustained, seconds, local):
+    """The headline GEMM back to back for `seconds` under the power cap (rotating input
+    sets), clocks sampled throughout; TFLOP/s over the whole loop."""
+    import torch
+    flops = 2.0 * SQ ** 3
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(50):
+        gemm(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    per = ev0.elapsed_time(ev1) / 50 * 1e-3
+    n = max(100, int(seconds / per))
+    sampler = clock_sampler(dev, local)
+    sampler.period_s = 0.002 if isinstance(sampler, NvmlSampler) else 0.1
+    sampler.start()
+    ev0.record(stream)
+    for i in range(n):
+        gemm(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    tf = flops * n / (ms * 1e-3) / 1e12
+    return {"launches": n, "seconds": ms * 1e-3, "TFLOP/s": tf, "peak_sustained": fp4_peak_sustained,
+            "frac_of_sustained_peak": tf / fp4_peak_sustained, "frac_vs_nominal_13p5PF": tf / NOMINAL_FP4_TFLOPS,
+            "peak_source": "measured bf16_tflops_sustained x 6 (nominal fp4/bf16)", "clocks": clocks}
 
 
 if __name__ == "__main__":

@@ -80,16 +80,31 @@ DEVI uint32_t e2m1x8_encode(const float (&v)[8]) {
   return r;
 }
 
-// RN(x / d) given y = RN(1 / d): one Markstein correction of RN(x y), exact when x, d
-// and the quotient stay well inside the normal range; otherwise the IEEE division.
-// The fast path requires x, d and the quotient all in [1e-30, 1e30] in magnitude, so that
-// no intermediate over- or underflows (the remainder stays a normal number).
+// Correctly rounded x / d without a division instruction, given y = RN(1 / d):
+//   q0 = RN(x y);  q1 = RN(q0 + RN(x - q0 d) y);  q2 = RN(q1 + (x - q1 d) y)  (fma each).
+// Why q2 = RN(x / d), with u = 2^-24 and no over- or underflow:
+//   y = (1 + h) / d and q0 = (x / d)(1 + e), |h| <= u, |e| <= 2u + u^2. The remainder's exact
+//   value is -x e; its rounding adds (1 + r), |r| <= u. So q0 + RN(x - q0 d) y =
+//   (x / d)(1 - e (r + h + r h)), within 5 u^2 relative of x / d, and q1, its rounding, is
+//   within half an ulp plus 5 u^2 of x / d: one of the two floats around it (faithful).
+//   For a faithful q1 the remainder x - q1 d is a float (one fma computes it exactly), and
+//   Markstein's theorem (P. Markstein, "Computation of elementary functions on the IBM
+//   RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990: a faithful quotient and a
+//   reciprocal within half an ulp give the correctly rounded quotient after one such
+//   correction) makes q2 = RN(x / d).
+// One correction alone is not enough: q0 itself can be two ulps off when the quotient's
+// significand is close to 2, and then the theorem does not apply.
+// Range: x, the quotient and d in [1e-30, 1e30] in magnitude keep d, y and every quotient
+// normal and the remainders representable: x - q d is a multiple of ulp(q) ulp(d) >=
+// 2^(e - 47) for 2^e <= |x| < 2^(e+1), hence of 2^-149 once |x| >= 2^-102 (~2e-31), so
+// even a subnormal remainder is exact. Elsewhere the IEEE division.
 DEVI float div_rn_by(float x, float d, float y) {
   const float q0 = __fmul_rn(x, y);
   const float ax = fabsf(x), aq = fabsf(q0);
   if (!(ax >= 1e-30f && ax <= 1e30f && aq >= 1e-30f && aq <= 1e30f && d >= 1e-30f && d <= 1e30f))
     return __fdiv_rn(x, d);
-  return __fmaf_rn(__fmaf_rn(-q0, d, x), y, q0);
+  const float q1 = __fmaf_rn(__fmaf_rn(-q0, d, x), y, q0);
+  return __fmaf_rn(__fmaf_rn(-q1, d, x), y, q1);
 }
 
 // g_inv = RN(1 / g), computed once per thread.
@@ -105,10 +120,12 @@ DEVI void quantize_block(const uint32_t (&w)[8], float g, float g_inv, uint32_t&
   uint32_t packed[2] = {0u, 0u};
   if (s != 0) {
     const float d = __fmul_rn(e4m3_decode(s), g);
-    // x / d correctly rounded without a division per element: y = RN(1/d), q0 = RN(x y)
-    // is within one ulp of x / d, the remainder x - q0 d is exact (fma), and
-    // RN(q0 + rem * y) = RN(x / d) by Markstein's theorem when nothing over- or
-    // underflows. Blocks outside that range take IEEE division.
+    // x / d correctly rounded without a division per element, by the two corrections of
+    // div_rn_by, two elements per instruction. The block-wide guard bounds d and the
+    // largest quotient; an element with |x| < 2^-102 or a quotient below 2^-126 may lose
+    // exactness, but its quotient is then below 2^-102 / 1e-30 < 0.2 (or 2^-126), so its
+    // code is 0 (with x's sign, restored below) whatever the rounding. Blocks outside the
+    // guard take IEEE division.
     const float y = __frcp_rn(d);
     const bool fast = d > 1e-30f && d < 1e30f && __fmul_rn(amax, y) < 1e30f;
     const uint64_t yy = f2(y, y), nd = f2(-d, -d);
@@ -121,8 +138,9 @@ DEVI void quantize_block(const uint32_t (&w)[8], float g, float g_inv, uint32_t&
         if (fast) {
           const uint64_t xx = f2(lo, hi);
           const uint64_t q0 = f2_mul(xx, yy);
-          const uint64_t rem = f2_fma(q0, nd, xx);  // x - q0 d, exact
-          f2_split(f2_fma(rem, yy, q0), v[2 * jj], v[2 * jj + 1]);
+          const uint64_t q1 = f2_fma(f2_fma(q0, nd, xx), yy, q0);  // faithful
+          const uint64_t rem = f2_fma(q1, nd, xx);                  // x - q1 d, exact
+          f2_split(f2_fma(rem, yy, q1), v[2 * jj], v[2 * jj + 1]);
           v[2 * jj] = with_sign_of(v[2 * jj], lo);
           v[2 * jj + 1] = with_sign_of(v[2 * jj + 1], hi);
         } else {

@@ -98,13 +98,24 @@ def test_decode_workload_full_size(M):
     check_gemm(y, A, B, cols=cols)
 
 
+def _every_tile_sample(M, N, seed):
+    """Rows: one random row in every 32-row group (each TMEM lane quarter of each CTA of
+    every 256-row tile, random lanes); columns: one random column in every 64-column group
+    (each column half of every 256-column tile and both 64-column store boxes in it)."""
+    rng = np.random.default_rng(seed)
+    rows = np.arange(0, M, 32) + rng.integers(0, 32, (M + 31) // 32)
+    cols = np.arange(0, N, 64) + rng.integers(0, 64, (N + 63) // 64)
+    rows = np.unique(np.concatenate([np.minimum(rows, M - 1), [0, M - 1]]))
+    cols = np.unique(np.concatenate([np.minimum(cols, N - 1), [0, N - 1]]))
+    return rows, cols
+
+
 def test_square_workload_sampled():
-    # M = N = K = 8192 in the benchmark's launch configuration; sampled rows x cols
+    # M = N = K = 8192 in the benchmark's launch configuration; a sample that reaches every
+    # 256 x 256 tile, every epilogue warp's rows and every output store box
     A, B = dense_case(8192, 8192, 8192, 1, 1.0, 1e-3, 0.02)
     y = _run(A, B)
-    rng = np.random.default_rng(0)
-    rows = np.concatenate([[0, 127, 128, 8191], rng.choice(8192, 60, replace=False)])
-    cols = np.concatenate([[0, 255, 256, 8191], rng.choice(8192, 124, replace=False)])
+    rows, cols = _every_tile_sample(8192, 8192, 0)
     check_gemm(y, A, B, rows=rows, cols=cols)
     # properties at full size: finite everywhere
     assert torch.isfinite(y.float()).all()
@@ -112,15 +123,41 @@ def test_square_workload_sampled():
 
 def test_prefill_workload_sampled():
     # prefill GEMM in the benchmark's configuration: x 4096 x 8192 (N(0,1) + 0.1% x20, seed 8)
-    # against W 28672 x 8192 (N(0, 0.02), seed 9); 112 column tiles, 23.6 tiles per CTA pair
+    # against W 28672 x 8192 (N(0, 0.02), seed 9); 1792 tiles of 256 x 256, 23.6 per CTA pair;
+    # the sample reaches every tile, epilogue warp and store box
     A = Operand(synth.normal_bf16((4096, 8192), 8, 1.0, 1e-3))
     B = Operand(synth.normal_bf16((28672, 8192), 9, 0.02))
     y = _run(A, B)
-    rng = np.random.default_rng(4)
-    rows = np.concatenate([[0, 255, 256, 4095], rng.choice(4096, 44, replace=False)])
-    cols = np.concatenate([[0, 255, 256, 28671], rng.choice(28672, 92, replace=False)])
+    rows, cols = _every_tile_sample(4096, 28672, 4)
     check_gemm(y, A, B, rows=rows, cols=cols)
     assert torch.isfinite(y.float()).all()
+
+
+# The smallest shapes the library accepts: K of one to three 64-element MMA steps (one
+# partial 256-element stage), N below one 128-row weight tile or one 64-column store box.
+SMALL_K = [64, 128, 192]
+SMALL_N = [8, 16, 72, 120]
+
+
+@pytest.mark.parametrize("K", SMALL_K)
+@pytest.mark.parametrize("N", SMALL_N)
+@pytest.mark.parametrize("kernel,bn", TILE_KERNELS)
+@pytest.mark.parametrize("M", [1, 16, 200])
+def test_tile_kernels_smallest_shapes(M, kernel, bn, N, K):
+    A, B = dense_case(M, N, K, 15, 1.0, 1e-3, 0.02)
+    m.nvfp4_tune(m.NVFP4_TUNE_STREAM_MAX_M, -1)
+    m.nvfp4_tune(m.NVFP4_TUNE_DENSE_KERNEL, kernel)
+    m.nvfp4_tune(m.NVFP4_TUNE_DENSE_BN, bn)
+    check_gemm(_run(A, B), A, B)
+
+
+@pytest.mark.parametrize("K", SMALL_K)
+@pytest.mark.parametrize("N", SMALL_N)
+@pytest.mark.parametrize("M,split", [(1, 0), (16, 0), (16, 3), (77, 1)])
+def test_stream_kernel_smallest_shapes(M, split, N, K):
+    A, B = dense_case(M, N, K, 16, 1.0, 1e-3, 0.02)
+    m.nvfp4_tune(m.NVFP4_TUNE_STREAM_SPLIT, split)
+    check_gemm(_run(A, B), A, B)
 
 
 @pytest.mark.parametrize("M,N,K,max_m", [

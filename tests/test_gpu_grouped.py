@@ -96,6 +96,15 @@ def test_grouped_many_experts():
     g.check(g.run())
 
 
+@pytest.mark.parametrize("K", [64, 128, 192])
+@pytest.mark.parametrize("N", [8, 16, 72, 120])
+def test_grouped_smallest_shapes(N, K):
+    # N below one 128-row weight tile (the tile's box then also covers the next experts'
+    # rows, whose outputs are never stored) and K of one partial 256-element stage
+    g = Grouped((3, 0, 17, 1, 70), N, K, 26)
+    g.check(g.run())
+
+
 def test_grouped_ragged_n_and_k():
     g = Grouped((10, 40, 0, 7), 136, 1088, 22)
     g.check(g.run())

@@ -145,3 +145,73 @@ def test_quantize_quotients_near_every_rounding_boundary():
             x[r, b * 16:(b + 1) * 16] = blk
     xb = synth.f32_to_bf16_bits(x)
     _quantize_and_compare(xb, g)
+
+
+def _global_scales_for_division_sweep():
+    rng = np.random.default_rng(2024)
+    g = list(np.float32(2.0 ** rng.uniform(-60.0, 60.0, 320)))
+    g += [np.float32(v) for v in (2.0 ** -10, 1.0, 2.0 ** 10, 1.0 / 2688, 20.0 / 2688, 0.08 / 2688)]
+    # the fast path's guard edges: block scales d = E4M3(s) g landing around 1e-30 and 1e30
+    for s in (1, 8, 56, 100, 126):
+        v = oracle.e4m3_value(s)
+        for edge in (1e-30, 1e30):
+            c = np.float32(edge / v)
+            g += [c, np.nextafter(c, np.float32(0)), np.nextafter(c, np.float32(np.inf))]
+    g += [np.float32(v) for v in (1e-30, 1e30, 1e-36, 1e36)]
+    return [x for x in g if np.isfinite(x) and x > 0]
+
+
+def _blocks_for_every_quotient(g):
+    """For each E4M3 scale code s a block maximum A (the largest bf16 at or below
+    6 g E4M3(s)), then every bf16 magnitude in [A / 64, A] with both signs (the
+    quotients from 0.09 to 6.x, where the E2M1 code can change), 15 per block after
+    a leading +-A, plus a few smaller values down to subnormals and zero."""
+    rng = np.random.default_rng(int(np.float32(g).view(np.uint32)))
+    blocks = []
+    for s in range(1, 127):
+        a64 = 6.0 * float(g) * oracle.e4m3_value(s)
+        if not a64 < 3.0e38:  # beyond bf16's finite range
+            continue
+        a = np.float32(a64)
+        a_bits = int(a.view(np.uint32)) >> 16  # round down to bf16
+        if a_bits == 0 or a_bits >= 0x7F80:
+            continue
+        lo = np.float32(float(synth.bf16_bits_to_f32(np.array([a_bits], np.uint16))[0]) / 64.0)
+        lo_bits = max(1, (int(lo.view(np.uint32)) + 0xFFFF) >> 16)
+        mags = np.arange(lo_bits, a_bits + 1, dtype=np.uint32)
+        small = rng.integers(0, max(lo_bits, 2), 24, dtype=np.uint32)
+        vals = np.concatenate([mags, mags | 0x8000, small, small | 0x8000]).astype(np.uint16)
+        rng.shuffle(vals)
+        n = (len(vals) + 14) // 15
+        vals = np.concatenate([vals, np.zeros(n * 15 - len(vals), np.uint16)]).reshape(n, 15)
+        lead = np.where(rng.random(n) < 0.5, a_bits, a_bits | 0x8000).astype(np.uint16)
+        blocks.append(np.concatenate([lead[:, None], vals], axis=1))
+    return np.concatenate(blocks) if blocks else np.zeros((0, 16), np.uint16)
+
+
+def test_quantize_division_exact_for_every_bf16_quotient():
+    # The quantiser divides without a division instruction (reciprocal + two fma
+    # corrections, correctly rounded by Markstein's theorem inside a guarded range, IEEE
+    # division outside it). Over 350 global scales (random over 2^+-60 and the guard's
+    # edges) and every E4M3 block scale, every bf16 element whose quotient can decide an
+    # E2M1 code is quantised and compared with the oracle's IEEE division, bit for bit.
+    K = 2048
+    per_row = K // 16
+    mismatches = 0
+    for g in _global_scales_for_division_sweep():
+        blk = _blocks_for_every_quotient(g)
+        if len(blk) == 0:
+            continue
+        rows = (len(blk) + per_row - 1) // per_row
+        xb = np.zeros((rows * per_row, 16), np.uint16)
+        xb[:len(blk)] = blk
+        xb = xb.reshape(rows, K)
+        x = to_dev(xb)
+        gd = torch.tensor([float(g)], dtype=torch.float32, device=dev())
+        q, sf = m.nvfp4_quantize(x, gd)
+        qo, sfo, _ = oracle.quantize(xb, np.float32(g))
+        qg, sfg = q.cpu().numpy(), sf.cpu().numpy()
+        bad = int((qg != qo).sum() + (sfg != sfo).sum())
+        assert bad == 0, f"g = {float(g)!r}: {bad} code or scale bytes differ"
+        mismatches += bad
+    assert mismatches == 0
