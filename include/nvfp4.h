@@ -270,6 +270,9 @@ int nvfp4_encode_e4m3(const float* v, int64_t n, uint8_t* out, void* stream);
  *                              "The Moment of Recalibration", The Broader Narrative Arc). Lines
  *                              keep the priority they were last loaded with; a later call with
  *                              0 on the same matrix demotes them again. Results are unchanged.
+ *   NVFP4_TUNE_DENSE_RASTER    order in which the persistent large-M kernels walk the output
+ *                              tiles: 0 (default) m-blocks fastest, -1 n-blocks fastest, G > 0
+ *                              bands of G m-blocks (m fastest inside a band). Results unchanged.
  * Returns NVFP4_OK or NVFP4_ERR_INVALID_ARG.
  */
 enum {
@@ -282,7 +285,8 @@ enum {
   NVFP4_TUNE_GROUPED_STAGES = 7,
   NVFP4_TUNE_DENSE_KERNEL = 8,
   NVFP4_TUNE_PDL = 9,
-  NVFP4_TUNE_WEIGHT_L2 = 10
+  NVFP4_TUNE_WEIGHT_L2 = 10,
+  NVFP4_TUNE_DENSE_RASTER = 11
 };
 int nvfp4_tune(int key, int value);
 

@@ -44,7 +44,7 @@ thread_local int g_last_launches = 0;
 
 struct Tune {
   int dense_bn = 0, dense_grid = 0, stream_max_m = 0, stream_split = 0, stream_stages = 0, grouped_grid = 0,
-      grouped_stages = 0, dense_kernel = 0, pdl = 0, weight_l2 = 0;
+      grouped_stages = 0, dense_kernel = 0, pdl = 0, weight_l2 = 0, dense_raster = 0;
 } g_tune;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -218,6 +218,10 @@ int nvfp4_tune(int key, int value) {
       if (value < 0 || value > 1) return NVFP4_ERR_INVALID_ARG;
       g_tune.weight_l2 = value;
       return NVFP4_OK;
+    case NVFP4_TUNE_DENSE_RASTER:
+      if (value < -1 || value > 1024) return NVFP4_ERR_INVALID_ARG;
+      g_tune.dense_raster = value;
+      return NVFP4_OK;
 
     default:
       return NVFP4_ERR_INVALID_ARG;
@@ -369,6 +373,7 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
     if ((rc = encode_sf(&tmSFB, sfb, nvfp4_scale_bytes(N, K) / 512))) return rc;
     if ((rc = encode_out(&tmY, y, M, N))) return rc;
     DenseArgs da = {sfa, sfb, ga, gb, y, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), dev_status};
+    da.raster = g_tune.dense_raster;
     const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
     int pairs = (g_tune.dense_grid ? g_tune.dense_grid : d.sms) / 2;
     if (pairs > tiles) pairs = static_cast<int>(tiles);
@@ -382,6 +387,7 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
   if ((rc = encode_2d(&tmA, a, M, K / 2, 128))) return rc;
   if ((rc = encode_2d(&tmB, b, N, K / 2, bn))) return rc;
   DenseArgs da = {sfa, sfb, ga, gb, y, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), dev_status};
+  da.raster = g_tune.dense_raster;
   const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
   int grid = g_tune.dense_grid ? g_tune.dense_grid : d.sms;
   if (grid > tiles) grid = static_cast<int>(tiles);
@@ -414,6 +420,7 @@ int nvfp4_gemm_quantize_out(const uint8_t* a, const uint8_t* sfa, const float* g
   tmY = tmA;  // unused by the quantising epilogue
   DenseArgs da = {sfa, sfb, ga, gb, nullptr, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                   dev_status, q_out, sf_out, g_out};
+  da.raster = g_tune.dense_raster;
   const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
   int pairs = (g_tune.dense_grid ? g_tune.dense_grid : d.sms) / 2;
   if (pairs > tiles) pairs = static_cast<int>(tiles);

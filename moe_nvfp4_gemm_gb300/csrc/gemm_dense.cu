@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     int issued_phase[STAGES];
     for (int i = 0; i < STAGES; ++i) issued_phase[i] = -1;
     for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
-      const int m_blk = t % mt, n_blk = t / mt;
+      int m_blk, n_blk;
+      tile_coords(t, mt, nt, p.raster, m_blk, n_blk);
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag)) break;
         if (elect_one()) {
@@ -195,7 +196,8 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     const bool wide = N % 16 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 31) == 0;
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
-      const int m_blk = t % mt, n_blk = t / mt;
+      int m_blk, n_blk;
+      tile_coords(t, mt, nt, p.raster, m_blk, n_blk);
       if (!mbar_wait_warp(tfull, acc_ph, abort_flag)) break;
       tc_fence_after();
       const int row = m_blk * 128 + q * 32 + lane;
@@ -299,7 +301,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     int issued_phase[STAGES];
     for (int i = 0; i < STAGES; ++i) issued_phase[i] = -1;
     for (int t = pair; t < tiles && !*abort_flag; t += npairs) {
-      const int m_blk = t % mt, n_blk = t / mt;
+      int m_blk, n_blk;
+      tile_coords(t, mt, nt, p.raster, m_blk, n_blk);
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag)) break;
         if (elect_one()) {
@@ -417,7 +420,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
     uint32_t acc_ph = 0;
     for (int t = pair; t < tiles; t += npairs) {
-      const int m_blk = t % mt, n_blk = t / mt;
+      int m_blk, n_blk;
+      tile_coords(t, mt, nt, p.raster, m_blk, n_blk);
       if (!mbar_wait_warp(tfull, acc_ph, abort_flag)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;

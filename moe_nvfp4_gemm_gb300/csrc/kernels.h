@@ -20,7 +20,28 @@ struct DenseArgs {
   uint8_t* q_out;
   uint8_t* sf_out;
   const float* g_out;
+  // tile order: 0 m-blocks fastest; -1 n-blocks fastest; G > 0 bands of G m-blocks, m fastest
+  // inside a band (the band's B tiles are read by G CTA pairs at about the same time)
+  int raster;
 };
+
+// Tile t of an mt x nt grid of output tiles in the order `raster` selects.
+__host__ __device__ inline void tile_coords(int t, int mt, int nt, int raster, int& m_blk, int& n_blk) {
+  if (raster < 0) {
+    m_blk = t / nt;
+    n_blk = t % nt;
+  } else if (raster == 0 || raster >= mt) {
+    m_blk = t % mt;
+    n_blk = t / mt;
+  } else {
+    const int band = t / (raster * nt);
+    const int first = band * raster;
+    const int rows = mt - first < raster ? mt - first : raster;
+    const int local = t - band * raster * nt;
+    m_blk = first + local % rows;
+    n_blk = local / rows;
+  }
+}
 
 struct StreamArgs {
   const uint8_t* sfw;      // weight scales (grouped: expert e at sfw + e * sfw_stride)

@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(autouse=True)
 def _reset_tuning():
     yield
-    for key in range(1, 11):
+    for key in range(1, 12):
         m.nvfp4_tune(key, 0)
 
 
@@ -59,6 +59,19 @@ def test_tile_kernel_persistent_loop_small_grid(kernel, grid):
     m.nvfp4_tune(m.NVFP4_TUNE_STREAM_MAX_M, -1)
     m.nvfp4_tune(m.NVFP4_TUNE_DENSE_KERNEL, kernel)
     m.nvfp4_tune(m.NVFP4_TUNE_DENSE_GRID, grid)
+    check_gemm(_run(A, B), A, B)
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("raster", [-1, 3, 64])
+def test_tile_kernel_raster_orders(kernel, raster):
+    # every tile order (n fastest, bands of 3 m-blocks with a ragged last band, one band)
+    # visits each output tile exactly once
+    A, B = dense_case(1800, 1288, 512, 17, 1.0, 1e-3, 0.02)
+    m.nvfp4_tune(m.NVFP4_TUNE_STREAM_MAX_M, -1)
+    m.nvfp4_tune(m.NVFP4_TUNE_DENSE_KERNEL, kernel)
+    m.nvfp4_tune(m.NVFP4_TUNE_DENSE_GRID, 10)
+    m.nvfp4_tune(m.NVFP4_TUNE_DENSE_RASTER, raster)
     check_gemm(_run(A, B), A, B)
 
 
