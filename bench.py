@@ -680,10 +680,58 @@ def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
     ms = time_graph(lambda i: m.nvfp4_grouped_gemm_swiglu(qa, sfa, ga, qb, sfb, gb, off_d, E, Mt, N, K,
                                                           y=y_act, workspace=wsp), 4, 5, stream)
     gbs = mbytes / (ms * 1e-3) / 1e9
+    ms_gu = ms
     out["moe_gate_up_swiglu"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
                                  "bytes": mbytes, "out": f"bf16 [{Mt}, {N // 2}] = silu(gate) * up",
                                  "tflops": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12}
-    del y_act
+    # down projection over the same routing: the SwiGLU output (I = N / 2 = 2048) quantised on
+    # the GPU (amax + block quantise), then the grouped GEMM K = 2048 -> N = 6144
+    I, Nd = N // 2, 6144
+    qd = torch.empty((E, Nd, I // 2), dtype=torch.uint8, device=dev)
+    sd_bytes = m.nvfp4_scale_bytes(Nd, I)
+    sd = torch.empty((E, sd_bytes), dtype=torch.uint8, device=dev)
+    gd = torch.empty(E, dtype=torch.float32, device=dev)
+    for e in range(E):
+        wq, ws, g = quantize_dev(to_dev(synth.moe_expert_weight(e, Nd, I, 5)))
+        qd[e].copy_(wq)
+        sd[e].copy_(ws)
+        gd[e:e + 1].copy_(g)
+    amax_a = torch.empty(1, dtype=torch.float32, device=dev)
+    g_a = torch.empty(1, dtype=torch.float32, device=dev)
+    q_a = torch.empty((Mt, I // 2), dtype=torch.uint8, device=dev)
+    sf_a = torch.empty(m.nvfp4_scale_bytes(Mt, I), dtype=torch.uint8, device=dev)
+    aws = torch.empty(m.nvfp4_amax_workspace_bytes(Mt * I), dtype=torch.uint8, device=dev)
+    y_dn = torch.empty((Mt, Nd), dtype=torch.bfloat16, device=dev)
+    wsd = torch.empty(m.nvfp4_grouped_gemm_workspace_bytes(E, Mt, Nd, I), dtype=torch.uint8, device=dev)
+
+    def act_quantize(i):
+        m.nvfp4_amax(y_act, amax_a, g_a, aws)
+        m.nvfp4_quantize(y_act, g_a, q_a, sf_a)
+
+    def down(i):
+        m.nvfp4_grouped_gemm(q_a, sf_a, g_a, qd, sd, gd, off_d, E, Mt, Nd, I, y=y_dn, workspace=wsd)
+
+    def layer(i):
+        m.nvfp4_grouped_gemm_swiglu(qa, sfa, ga, qb, sfb, gb, off_d, E, Mt, N, K, y=y_act, workspace=wsp)
+        act_quantize(i)
+        down(i)
+
+    act_quantize(0)
+    ms_q = time_graph(act_quantize, 4, 5, stream)
+    ms_dn = time_graph(down, 4, 5, stream)
+    ms_layer = time_graph(layer, 2, 5, stream)
+    dbytes = hit * (Nd * I // 2 + sd_bytes)
+    gbs = dbytes / (ms_dn * 1e-3) / 1e9
+    out["moe_down"] = {"us": ms_dn * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm,
+                       "hbm_frac_vs_8TBps": gbs / NOMINAL_HBM_GBS, "experts_hit": hit, "bytes": dbytes,
+                       "shape": f"per expert K = {I} -> N = {Nd}, {Mt} routed rows",
+                       "tflops": 2.0 * Mt * Nd * I / (ms_dn * 1e-3) / 1e12,
+                       "act_amax_quantize_us": ms_q * 1e3,
+                       "layer_us": ms_layer * 1e3,
+                       "layer": "gate/up + SwiGLU, amax + quantise of the activation, down projection (one graph)",
+                       "layer_weight_GBps": (mbytes + dbytes) / (ms_layer * 1e-3) / 1e9,
+                       "layer_hbm_frac": (mbytes + dbytes) / (ms_layer * 1e-3) / 1e9 / hbm}
+    del y_act, qd, sd, y_dn
     a_s, off_s, _ = synth.moe_tokens(512, E, 8, K, 3, zipf_s=1.0)
     qs, sfs, gs = quantize_dev(to_dev(a_s))
     off_sd = to_dev(off_s)
