@@ -273,6 +273,14 @@ int nvfp4_encode_e4m3(const float* v, int64_t n, uint8_t* out, void* stream);
  *   NVFP4_TUNE_DENSE_RASTER    order in which the persistent large-M kernels walk the output
  *                              tiles: 0 (default) m-blocks fastest, -1 n-blocks fastest, G > 0
  *                              bands of G m-blocks (m fastest inside a band). Results unchanged.
+ *   NVFP4_TUNE_WATCHDOG_US     limit, in microseconds, after which a GEMM kernel's pipeline
+ *                              wait gives up, stops the CTA's other roles, frees its tensor
+ *                              memory and reports NVFP4_ERR_TIMEOUT in *dev_status (0: the
+ *                              default, 2 s). Applies to the launches that follow.
+ *   NVFP4_TUNE_TEST_WITHHOLD_STAGE  test hook for the timeout path: k >= 1 makes the first CTA
+ *                              of each GEMM kernel withhold the loads of the k-th pipeline stage
+ *                              it would request, so that stage never arrives and the waits run
+ *                              into the watchdog (the result is then unspecified). 0: off.
  * Returns NVFP4_OK or NVFP4_ERR_INVALID_ARG.
  */
 enum {
@@ -286,7 +294,9 @@ enum {
   NVFP4_TUNE_DENSE_KERNEL = 8,
   NVFP4_TUNE_PDL = 9,
   NVFP4_TUNE_WEIGHT_L2 = 10,
-  NVFP4_TUNE_DENSE_RASTER = 11
+  NVFP4_TUNE_DENSE_RASTER = 11,
+  NVFP4_TUNE_WATCHDOG_US = 12,
+  NVFP4_TUNE_TEST_WITHHOLD_STAGE = 13
 };
 int nvfp4_tune(int key, int value);
 

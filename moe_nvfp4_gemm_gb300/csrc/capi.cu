@@ -44,7 +44,7 @@ thread_local int g_last_launches = 0;
 
 struct Tune {
   int dense_bn = 0, dense_grid = 0, stream_max_m = 0, stream_split = 0, stream_stages = 0, grouped_grid = 0,
-      grouped_stages = 0, dense_kernel = 0, pdl = 0, weight_l2 = 0, dense_raster = 0;
+      grouped_stages = 0, dense_kernel = 0, pdl = 0, weight_l2 = 0, dense_raster = 0, watchdog_us = 0, withhold_stage = 0;
 } g_tune;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -140,6 +140,8 @@ int stream_pdl_mode() { return g_tune.pdl == 0 ? 2 : (g_tune.pdl < 0 ? 0 : g_tun
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
 
+uint64_t watchdog_ns() { return g_tune.watchdog_us ? uint64_t(g_tune.watchdog_us) * 1000u : kWatchdogNs; }
+
 int64_t pad16(int64_t v) { return (v + 15) / 16 * 16; }
 
 int pow2_at_least(int v) {
@@ -217,6 +219,14 @@ int nvfp4_tune(int key, int value) {
     case NVFP4_TUNE_WEIGHT_L2:
       if (value < 0 || value > 1) return NVFP4_ERR_INVALID_ARG;
       g_tune.weight_l2 = value;
+      return NVFP4_OK;
+    case NVFP4_TUNE_WATCHDOG_US:
+      if (value < 0) return NVFP4_ERR_INVALID_ARG;
+      g_tune.watchdog_us = value;
+      return NVFP4_OK;
+    case NVFP4_TUNE_TEST_WITHHOLD_STAGE:
+      if (value < 0) return NVFP4_ERR_INVALID_ARG;
+      g_tune.withhold_stage = value;
       return NVFP4_OK;
     case NVFP4_TUNE_DENSE_RASTER:
       if (value < -1 || value > 1024) return NVFP4_ERR_INVALID_ARG;
@@ -343,6 +353,8 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
     s.split = split;
     s.pdl = stream_pdl_mode();
     s.w_keep = g_tune.weight_l2;
+    s.watchdog_ns = watchdog_ns();
+    s.drop_stage = g_tune.withhold_stage;
     const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0) - 1536;
     const int recv_bytes = stream_recv_bytes(s.M, split);
     int stages = g_tune.stream_stages;
@@ -374,6 +386,8 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
     if ((rc = encode_out(&tmY, y, M, N))) return rc;
     DenseArgs da = {sfa, sfb, ga, gb, y, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), dev_status};
     da.raster = g_tune.dense_raster;
+    da.watchdog_ns = watchdog_ns();
+    da.drop_stage = g_tune.withhold_stage;
     const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
     int pairs = (g_tune.dense_grid ? g_tune.dense_grid : d.sms) / 2;
     if (pairs > tiles) pairs = static_cast<int>(tiles);
@@ -388,6 +402,8 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
   if ((rc = encode_2d(&tmB, b, N, K / 2, bn))) return rc;
   DenseArgs da = {sfa, sfb, ga, gb, y, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), dev_status};
   da.raster = g_tune.dense_raster;
+  da.watchdog_ns = watchdog_ns();
+  da.drop_stage = g_tune.withhold_stage;
   const int64_t tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
   int grid = g_tune.dense_grid ? g_tune.dense_grid : d.sms;
   if (grid > tiles) grid = static_cast<int>(tiles);
@@ -421,6 +437,8 @@ int nvfp4_gemm_quantize_out(const uint8_t* a, const uint8_t* sfa, const float* g
   DenseArgs da = {sfa, sfb, ga, gb, nullptr, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
                   dev_status, q_out, sf_out, g_out};
   da.raster = g_tune.dense_raster;
+  da.watchdog_ns = watchdog_ns();
+  da.drop_stage = g_tune.withhold_stage;
   const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
   int pairs = (g_tune.dense_grid ? g_tune.dense_grid : d.sms) / 2;
   if (pairs > tiles) pairs = static_cast<int>(tiles);
@@ -527,6 +545,8 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   s.split = 1;
   s.pdl = stream_pdl_mode();
   s.w_keep = g_tune.weight_l2;
+  s.watchdog_ns = watchdog_ns();
+  s.drop_stage = g_tune.withhold_stage;
   s.x_rows = kGroupTileRows;
   s.acc_cols = kGroupTileRows;
   s.acc_bufs = 2;

@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t wd = p.watchdog_ns;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -104,12 +105,14 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     uint32_t ph = 0;
     int issued_phase[STAGES];
     for (int i = 0; i < STAGES; ++i) issued_phase[i] = -1;
+    int issued = 0;
     for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
       int m_blk, n_blk;
       tile_coords(t, mt, nt, p.raster, m_blk, n_blk);
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag)) break;
-        if (elect_one()) {
+        if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag, wd)) break;
+        const bool withheld = blockIdx.x == 0 && ++issued == p.drop_stage;  // test hook
+        if (!withheld && elect_one()) {
           const int nsub = min(4, (K - kb * 256) / 64);
           uint8_t* st = smem + s * C::STAGE_BYTES;
           int ngroups = 0;
@@ -139,17 +142,17 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     for (int i = 0; i < STAGES; ++i)
       if (issued_phase[i] >= 0) {
         volatile int32_t dummy = 0;
-        mbar_wait_warp(&full[i], issued_phase[i], &dummy);
+        mbar_wait_warp(&full[i], issued_phase[i], &dummy, wd);
       }
   } else if (warp == 1) {
     const uint32_t idesc = idesc_nvf4(128, BN);
     int s = 0;
     uint32_t ph = 0, acc_ph = 0;
     for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
-      if (!mbar_wait_warp(tempty, acc_ph ^ 1, abort_flag)) break;
+      if (!mbar_wait_warp(tempty, acc_ph ^ 1, abort_flag, wd)) break;
       tc_fence_after();
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait_warp(&full[s], ph, abort_flag)) break;
+        if (!mbar_wait_warp(&full[s], ph, abort_flag, wd)) break;
         tc_fence_after();
         if (elect_one()) {
           const int nsub = min(4, (K - kb * 256) / 64);
@@ -188,7 +191,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     if (elect_one()) tc_commit(drain);
     __syncwarp();
     volatile int32_t dummy = 0;
-    mbar_wait_warp(drain, 0, &dummy);
+    mbar_wait_warp(drain, 0, &dummy, wd);
   } else {
     const int q = warp & 3;         // TMEM lane quarter this warp may read
     const int h = (warp - 2) >> 2;  // which half of the tile's columns
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
       int m_blk, n_blk;
       tile_coords(t, mt, nt, p.raster, m_blk, n_blk);
-      if (!mbar_wait_warp(tfull, acc_ph, abort_flag)) break;
+      if (!mbar_wait_warp(tfull, acc_ph, abort_flag, wd)) break;
       tc_fence_after();
       const int row = m_blk * 128 + q * 32 + lane;
       drain_accumulator<BN / 2>(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * (BN / 2), alpha,
@@ -259,6 +262,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t wd = p.watchdog_ns;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   if (threadIdx.x == 0) {
@@ -300,12 +304,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     uint32_t ph = 0;
     int issued_phase[STAGES];
     for (int i = 0; i < STAGES; ++i) issued_phase[i] = -1;
+    int issued = 0;
     for (int t = pair; t < tiles && !*abort_flag; t += npairs) {
       int m_blk, n_blk;
       tile_coords(t, mt, nt, p.raster, m_blk, n_blk);
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag)) break;
-        if (elect_one()) {
+        if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag, wd)) break;
+        // test hook: the even CTA of the first pair withholds its expect-tx arrival and
+        // loads, so that stage's barrier never completes
+        const bool withheld = blockIdx.x == 0 && ++issued == p.drop_stage;
+        if (!withheld && elect_one()) {
           uint8_t* st = smem + s * C::STAGE_BYTES;
           const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
           if (leader) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE_BYTES);
@@ -331,7 +339,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       for (int i = 0; i < STAGES; ++i)
         if (issued_phase[i] >= 0) {
           volatile int32_t dummy = 0;
-          mbar_wait_warp(&full[i], issued_phase[i], &dummy);
+          mbar_wait_warp(&full[i], issued_phase[i], &dummy, wd);
         }
   } else if (warp == kWaiterWarp) {
     // Owns every wait in front of the MMA warp: the accumulator being free at the
@@ -345,11 +353,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       uint32_t ph = 0, acc_ph = 0;
       for (int t = pair; t < tiles; t += npairs) {
         const bool tile_ok =
-            __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(tempty, acc_ph ^ 1, abort_flag);
+            __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(tempty, acc_ph ^ 1, abort_flag, wd);
         acc_ph ^= 1;
         for (int kb = 0; kb < KB; ++kb) {
           const bool ok =
-              tile_ok && __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(&full[s], ph, abort_flag);
+              tile_ok && __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(&full[s], ph, abort_flag, wd);
           named_sync_and(kStageHandoffBarrier, 64, ok);
           if (++s == STAGES) {
             s = 0;
@@ -405,7 +413,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       if (elect_one()) tc_commit_pair(drain, 1);
       __syncwarp();
       volatile int32_t dummy = 0;
-      mbar_wait_warp(drain, 0, &dummy);
+      mbar_wait_warp(drain, 0, &dummy, wd);
     }
   } else {
     const int q = warp & 3, h = (warp - 2) >> 2;
@@ -422,7 +430,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     for (int t = pair; t < tiles; t += npairs) {
       int m_blk, n_blk;
       tile_coords(t, mt, nt, p.raster, m_blk, n_blk);
-      if (!mbar_wait_warp(tfull, acc_ph, abort_flag)) break;
+      if (!mbar_wait_warp(tfull, acc_ph, abort_flag, wd)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
       const int row0 = m_blk * 256 + rank * 128 + q * 32;

@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t wd = p.watchdog_ns;
   const int N = p.N, K = p.K;
   const int NT = (N + 127) / 128;
   const int KB = (K + 255) / 256;
@@ -215,7 +216,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     // costs this thread ~0.6 us), so that none of the matrix is left at normal priority.
     const uint64_t keep = p.w_keep ? policy_evict_last() : 0;
     if (p.pdl == 2) griddep_wait();  // set-up-only overlap: no load before the previous kernel completes
-    for (int j = 0; j < n_pre; ++j) issue_stage(j, first_it.kb0 + j, src, p.pdl != 1, p.w_keep != 0, keep, keep);
+    for (int j = 0; j < n_pre; ++j)
+      if (!(blockIdx.x == 0 && j + 1 == p.drop_stage))  // test hook: stage withheld
+        issue_stage(j, first_it.kb0 + j, src, p.pdl != 1, p.w_keep != 0, keep, keep);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, p.tmem_cols);
@@ -287,7 +290,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         if (tok_ready) tok_regs = load_tokens(nx);
       }
       for (int kb = it.kb0; kb < it.kb1; ++kb) {
-        if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag)) break;
+        if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag, wd)) break;
         if (!have_pol && issued >= STAGES && *policies_ready) {
           __threadfence_block();
           pol_w = policies[0];
@@ -296,7 +299,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         }
         const bool pre = issued < n_pre;  // requested in the prologue
         ++issued;
-        if (!pre && elect_one()) issue_stage(s, kb, src, !pending, have_pol, pol_w, pol_x);
+        const bool withheld = blockIdx.x == 0 && issued == p.drop_stage;  // test hook
+        if (!pre && !withheld && elect_one()) issue_stage(s, kb, src, !pending, have_pol, pol_w, pol_x);
         __syncwarp();
         if (pending) {
           pend_stage[npend] = s;
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     for (int i = 0; i < STAGES; ++i)
       if (issued_phase[i] >= 0) {
         volatile int32_t dummy = 0;
-        mbar_wait_warp(&full[i], issued_phase[i], &dummy);
+        mbar_wait_warp(&full[i], issued_phase[i], &dummy, wd);
       }
   } else if (warp == kStreamWaiterWarp) {
     // Owns every wait in front of the MMA warp (the item's accumulator buffer being
@@ -343,12 +347,12 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     Item it;
     for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it); i += stride) {
       const bool item_ok =
-          __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(&tempty[buf], acc_ph[buf] ^ 1, abort_flag);
+          __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(&tempty[buf], acc_ph[buf] ^ 1, abort_flag, wd);
       acc_ph[buf] ^= 1;
       buf = (buf + 1 == p.acc_bufs) ? 0 : buf + 1;
       for (int kb = it.kb0; kb < it.kb1; ++kb) {
         const bool ok =
-            item_ok && __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(&full[s], ph, abort_flag);
+            item_ok && __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(&full[s], ph, abort_flag, wd);
         named_sync_and(kStreamHandoffBarrier, 64, ok);
         if (++s == STAGES) {
           s = 0;
@@ -404,7 +408,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     if (elect_one()) tc_commit(drain);
     __syncwarp();
     volatile int32_t dummy = 0;
-    mbar_wait_warp(drain, 0, &dummy);
+    mbar_wait_warp(drain, 0, &dummy, wd);
   } else {
     constexpr int MAXC = kGroupTile;
     if (warp == 2) {
@@ -428,7 +432,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     uint32_t acc_ph[2] = {0, 0};
     Item it;
     for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it); i += stride) {
-      if (!mbar_wait_warp(&tfull[buf], acc_ph[buf], abort_flag)) break;
+      if (!mbar_wait_warp(&tfull[buf], acc_ph[buf], abort_flag, wd)) break;
       tc_fence_after();
       const float alpha = ga * (GROUPED ? __ldg(p.gb + it.e) : gb0);
       const int wrow = it.wt * 128 + q * 32 + lane;  // output column
@@ -522,7 +526,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
       __syncwarp();
     }
     const int mine = min(m_own, p.M - static_cast<int>(rank) * m_own);
-    if (mine > 0 && mbar_wait_warp(red_bar, 0, abort_flag)) {
+    // Every CTA sends its partials, also after an abort (then garbage), and each owner waits
+    // for all of them whatever its own state: no CTA may leave while a peer's copy into its
+    // shared memory is in flight. A sender that aborted sends once its own waits gave up (one
+    // limit after they began), so the owner's wait allows four limits before it gives up.
+    volatile int32_t no_abort = 0;
+    const bool received = mine > 0 && mbar_wait_warp(red_bar, 0, &no_abort, 4 * wd);
+    if (mine > 0 && !received) *abort_flag = 1;
+    if (received && !*abort_flag) {
       const int q = warp & 3;
       const int wrow = (blockIdx.x / S) * 128 + q * 32 + lane;
       const float alpha = dense_alpha;

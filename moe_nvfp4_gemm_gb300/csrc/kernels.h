@@ -20,6 +20,8 @@ struct DenseArgs {
   uint8_t* q_out;
   uint8_t* sf_out;
   const float* g_out;
+  uint64_t watchdog_ns;  // limit of every pipeline wait
+  int drop_stage;        // test hook: k >= 1 withholds the k-th stage CTA 0 loads (0: none)
   // tile order: 0 m-blocks fastest; -1 n-blocks fastest; G > 0 bands of G m-blocks, m fastest
   // inside a band (the band's B tiles are read by G CTA pairs at about the same time)
   int raster;
@@ -66,6 +68,8 @@ struct StreamArgs {
   const int32_t* row_token;  // grouped: routed row r reads token row row_token[r] of x (null: row r)
   int T;                     // grouped with row_token: rows of x
   int w_keep;                // weights loaded L2 evict_last (kept resident across calls), else evict_first
+  uint64_t watchdog_ns;      // limit of every pipeline wait
+  int drop_stage;            // test hook: k >= 1 withholds the k-th stage CTA 0 loads (0: none)
 };
 
 

@@ -14,7 +14,8 @@ namespace nvfp4 {
 // Device-side status codes (mirrors nvfp4_status in nvfp4.h).
 enum : int32_t { kStatusTimeout = -7, kStatusBadOffsets = -8 };
 
-// A wait that has not completed after this long gives up and reports a timeout.
+// A wait that has not completed after this long gives up and reports a timeout (the
+// default; every launch passes its own limit).
 constexpr uint64_t kWatchdogNs = 2000000000ull;
 
 DEVI uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -67,9 +68,9 @@ DEVI bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete. Gives up (returns
-// false) when *abort becomes non-zero or after kWatchdogNs, in which case it sets
+// false) when *abort becomes non-zero or after limit_ns, in which case it sets
 // *abort so that every other role of the CTA stops too.
-DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
+DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -78,7 +79,7 @@ DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(a, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWatchdogNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }
@@ -86,8 +87,8 @@ DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
 }
 
 // Warp-collective wait: every lane polls, the result is the same in all lanes.
-DEVI bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort)) != 0;
+DEVI bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int32_t* abort, uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, limit_ns)) != 0;
 }
 
 // Named CTA barrier `id` over `nthreads` threads (whole warps). Used in lockstep by

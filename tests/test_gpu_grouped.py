@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(autouse=True)
 def _reset_tuning():
     yield
-    for key in range(1, 12):
+    for key in range(1, 14):
         m.nvfp4_tune(key, 0)
 
 
