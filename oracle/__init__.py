@@ -95,6 +95,21 @@ def lib():
                                                ctypes.c_int64, _i64p, ctypes.c_int64,
                                                _f64p, _f64p]
             L.nvo_num_threads.restype = ctypes.c_int
+            L.nvo_prune_pairs.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int64, _u16p, _u8p]
+            L.nvo_meta_tiled_bytes.restype = ctypes.c_int64
+            L.nvo_meta_tiled_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+            L.nvo_meta_offset.restype = ctypes.c_int64
+            L.nvo_meta_offset.argtypes = [ctypes.c_int64] * 3
+            L.nvo_meta_tile.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p]
+            L.nvo_meta_untile.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p]
+            L.nvo_scale_bytes_bs.restype = ctypes.c_int64
+            L.nvo_scale_bytes_bs.argtypes = [ctypes.c_int64] * 3
+            L.nvo_quantize_b32.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
+                                           _u8p, _u8p]
+            L.nvo_sparse_gemm_f64.argtypes = [_u8p, _u8p, ctypes.c_float, _u8p, _u8p, _u8p, ctypes.c_float,
+                                              ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                              _i64p, ctypes.c_int64, _i64p, ctypes.c_int64,
+                                              _f64p, _f64p]
             _lib = L
     return _lib
 
@@ -298,6 +313,106 @@ def within_tolerance(y_gpu: np.ndarray, y_ref: np.ndarray, absdot: np.ndarray,
         ratio = np.where(bound > 0, err / bound, np.where(err > 0, np.inf, 0.0))
     worst = float(np.max(ratio)) if ratio.size else 0.0
     return bool(np.all(err <= bound)), worst
+
+
+# ---- pair-wise 2:4 sparsity ---------------------------------------------------------
+
+def prune_pairs(w_bits: np.ndarray):
+    """Pair-wise 2:4 pruning and compression of a bf16 [N, K] weight (K % 8 == 0): per
+    group of 8 K elements the two pairs with the largest |w_2j| + |w_2j+1| are kept (ties
+    to the lower pair index). Returns (c bf16 bits [N, K/2], meta [N, K/16] u8), meta
+    nibble per group = i0 | i1 << 2 of the kept pair indices, group 2b in the low nibble."""
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    N, K = w.shape
+    c = np.empty((N, K // 2), dtype=np.uint16)
+    meta = np.empty((N, K // 16), dtype=np.uint8)
+    lib().nvo_prune_pairs(_p(w, _u16p), N, K, _p(c, _u16p), _p(meta, _u8p))
+    return c, meta
+
+
+def meta_tiled_bytes(N: int, K: int) -> int:
+    return int(lib().nvo_meta_tiled_bytes(N, K))
+
+
+def meta_offset(n: int, b: int, K: int) -> int:
+    return int(lib().nvo_meta_offset(n, b, K))
+
+
+def meta_tile(meta: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Linear [N, K/16] metadata -> the tiled layout (4096-byte tile per 128 rows x 512 K)."""
+    lin = np.ascontiguousarray(meta, dtype=np.uint8)
+    out = np.empty(meta_tiled_bytes(N, K), dtype=np.uint8)
+    lib().nvo_meta_tile(_p(lin, _u8p), N, K, _p(out, _u8p))
+    return out
+
+
+def meta_untile(tiled: np.ndarray, N: int, K: int) -> np.ndarray:
+    t = np.ascontiguousarray(tiled, dtype=np.uint8)
+    out = np.empty((N, K // 16), dtype=np.uint8)
+    lib().nvo_meta_untile(_p(t, _u8p), N, K, _p(out, _u8p))
+    return out
+
+
+def sf_unswizzle_bs(sf: np.ndarray, rows: int, K: int, bs: int) -> np.ndarray:
+    """Tiled scale tensor with `bs`-element blocks -> linear [rows, K/bs] (numpy restatement
+    of the tile formula with K/bs scale columns)."""
+    kc = K // bs
+    kc4 = (kc + 3) // 4
+    r = np.arange(rows)[:, None]
+    c = np.arange(kc)[None, :]
+    off = ((r // 128) * kc4 + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (c % 4)
+    return np.asarray(sf)[off]
+
+
+def sf_swizzle_bs(lin: np.ndarray, rows: int, K: int, bs: int) -> np.ndarray:
+    kc = K // bs
+    kc4 = (kc + 3) // 4
+    r = np.arange(rows)[:, None]
+    c = np.arange(kc)[None, :]
+    off = ((r // 128) * kc4 + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (c % 4)
+    out = np.zeros((rows + 127) // 128 * 128 * kc4 * 4, dtype=np.uint8)
+    out[off] = lin
+    return out
+
+
+def scale_bytes_b32(rows: int, K: int) -> int:
+    return int(lib().nvo_scale_bytes_bs(rows, K, 32))
+
+
+def quantize_b32(x_bits: np.ndarray, g_fixed=None):
+    """The quantisation recipe with 32-element blocks (the dense operand of the sparse GEMM).
+    Returns (q [M, K/2], sf tiled over K/32 columns, g)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = x.shape
+    g = np.float32(global_scale(amax(x))) if g_fixed is None else np.float32(g_fixed)
+    q = np.empty((M, K // 2), dtype=np.uint8)
+    sf = np.empty(scale_bytes_b32(M, K), dtype=np.uint8)
+    lib().nvo_quantize_b32(_p(x, _u16p), M, K, float(g), _p(q, _u8p), _p(sf, _u8p))
+    return q, sf, g
+
+
+def sparse_quantize_weight(w_bits: np.ndarray):
+    """Prune, compress and quantise a bf16 weight [N, K]: returns (cq [N, K/4] u8 codes of
+    the compressed values, csf their tiled 16-block scales over K/2, g, meta [N, K/16])."""
+    c, meta = prune_pairs(w_bits)
+    cq, csf, g = quantize(c)
+    return cq, csf, g, meta
+
+
+def sparse_gemm(xq, xsf, gx, cq, csf, meta, gw, M: int, N: int, K: int, rows=None, cols=None):
+    """y = x . W^T in float64 with x in 32-element blocks and W pair-wise 2:4 sparse
+    (compressed codes cq, scales csf, metadata meta [N, K/16]); returns (y, absdot)."""
+    r_arr, nr, r_ptr = _opt_idx(rows)
+    c_arr, nc, c_ptr = _opt_idx(cols)
+    nr = M if rows is None else nr
+    nc = N if cols is None else nc
+    y = np.zeros((nr, nc), dtype=np.float64)
+    ad = np.zeros((nr, nc), dtype=np.float64)
+    xq, xsf, cq, csf, meta = (np.ascontiguousarray(a, dtype=np.uint8) for a in (xq, xsf, cq, csf, meta))
+    lib().nvo_sparse_gemm_f64(_p(xq, _u8p), _p(xsf, _u8p), float(gx), _p(cq, _u8p), _p(csf, _u8p),
+                              _p(meta, _u8p), float(gw), M, N, K, r_ptr, nr, c_ptr, nc,
+                              _p(y, _f64p), _p(ad, _f64p))
+    return y, ad
 
 
 def num_threads() -> int:

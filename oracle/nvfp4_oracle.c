@@ -334,6 +334,183 @@ int nvo_grouped_gemm_f64(const uint8_t* a, const uint8_t* sfa, float ga, const u
   return 0;
 }
 
+/* ---- pair-wise 2:4 sparsity (weights) ---------------------------------------
+ *
+ * The structured sparsity of the sparse tensor-core MMA on FP4 data: in every group of
+ * 8 consecutive K elements (4 pairs of neighbours 2j, 2j+1) two pairs are kept ("FP4
+ * structured sparsity", "The Moment of Recalibration", The Broader Narrative Arc; the
+ * pages give no format, the readings are the library's):
+ *   - pruning of a dense bf16 W: keep the two pairs with the largest score
+ *     |w_2j| + |w_2j+1| (one fp32 addition), a tie going to the lower pair index;
+ *   - compression: the kept pairs in increasing index order, [N, K/2] values;
+ *   - metadata: per group the nibble i0 | i1 << 2 (i0 < i1, the kept pair indices);
+ *     byte b of a row holds groups 2b (low nibble) and 2b + 1, [N, K/16] bytes;
+ *   - the compressed values are quantised as an ordinary [N, K/2] NVFP4 tensor
+ *     (16-element blocks over stored values = 32 logical K elements);
+ *   - the dense operand (activations) carries one scale per 32 K elements.
+ */
+
+static void top2_pairs(const uint16_t* grp, int* i0, int* i1) {
+  float sc[4];
+  for (int j = 0; j < 4; j++) sc[j] = fabsf(bf16_to_f32(grp[2 * j])) + fabsf(bf16_to_f32(grp[2 * j + 1]));
+  int best = 0;
+  for (int j = 1; j < 4; j++)
+    if (sc[j] > sc[best]) best = j;
+  int second = -1;
+  for (int j = 0; j < 4; j++)
+    if (j != best && (second < 0 || sc[j] > sc[second])) second = j;
+  *i0 = best < second ? best : second;
+  *i1 = best < second ? second : best;
+}
+
+/* w: bf16 [N, K] (K % 8 == 0). c: bf16 [N, K/2]. meta: [N, K/16] bytes. */
+void nvo_prune_pairs(const uint16_t* w, int64_t N, int64_t K, uint16_t* c, uint8_t* meta) {
+  memset(meta, 0, (size_t)(N * (K / 16)));
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; n++)
+    for (int64_t g = 0; g < K / 8; g++) {
+      const uint16_t* grp = w + n * K + g * 8;
+      int i0, i1;
+      top2_pairs(grp, &i0, &i1);
+      uint16_t* out = c + n * (K / 2) + g * 4;
+      out[0] = grp[2 * i0];
+      out[1] = grp[2 * i0 + 1];
+      out[2] = grp[2 * i1];
+      out[3] = grp[2 * i1 + 1];
+      meta[n * (K / 16) + g / 2] |= (uint8_t)((i0 | (i1 << 2)) << (4 * (g & 1)));
+    }
+}
+
+/* Tiled metadata: per 128 rows and 512 K elements (32 bytes a row) one 4096-byte tile,
+ * rows in groups of 8 with each row's 32 bytes as two 16-byte halves:
+ * byte b of row r at (r%128/8)*256 + (b/16)*128 + (r%8)*16 + b%16. */
+int64_t nvo_meta_tiled_bytes(int64_t N, int64_t K) { return (N + 127) / 128 * ((K + 511) / 512) * 4096; }
+
+int64_t nvo_meta_offset(int64_t n, int64_t b, int64_t K) {
+  int64_t kmc = (K + 511) / 512, r = n % 128, bb = b % 32;
+  return ((n / 128) * kmc + b / 32) * 4096 + (r / 8) * 256 + (bb / 16) * 128 + (r % 8) * 16 + bb % 16;
+}
+
+void nvo_meta_tile(const uint8_t* lin, int64_t N, int64_t K, uint8_t* tiled) {
+  memset(tiled, 0, (size_t)nvo_meta_tiled_bytes(N, K));
+  for (int64_t n = 0; n < N; n++)
+    for (int64_t b = 0; b < K / 16; b++) tiled[nvo_meta_offset(n, b, K)] = lin[n * (K / 16) + b];
+}
+
+void nvo_meta_untile(const uint8_t* tiled, int64_t N, int64_t K, uint8_t* lin) {
+  for (int64_t n = 0; n < N; n++)
+    for (int64_t b = 0; b < K / 16; b++) lin[n * (K / 16) + b] = tiled[nvo_meta_offset(n, b, K)];
+}
+
+/* Scale tensors with `bs`-element blocks (16 or 32): the same 128 x 4 tiles over K/bs columns. */
+int64_t nvo_scale_bytes_bs(int64_t rows, int64_t K, int64_t bs) {
+  int64_t kc = K / bs;
+  return ((rows + 127) / 128) * 128 * (((kc + 3) / 4) * 4);
+}
+
+static int64_t sf_offset_bs(int64_t r, int64_t c, int64_t K, int64_t bs) {
+  int64_t kc4 = (K / bs + 3) / 4;
+  return ((r / 128) * kc4 + c / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4);
+}
+
+/* The quantisation recipe of nvo_quantize with 32-element blocks. */
+void nvo_quantize_b32(const uint16_t* x, int64_t M, int64_t K, float g, uint8_t* q, uint8_t* sf) {
+  init_tables();
+  memset(sf, 0, (size_t)nvo_scale_bytes_bs(M, K, 32));
+  int64_t kc = K / 32;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < M; r++) {
+    for (int64_t c = 0; c < kc; c++) {
+      const uint16_t* blk = x + r * K + c * 32;
+      float amax = 0.0f;
+      for (int i = 0; i < 32; i++) {
+        float a = fabsf(bf16_to_f32(blk[i]));
+        if (a > amax) amax = a;
+      }
+      float t1 = amax / 6.0f;
+      float t = t1 / g;
+      int s = nvo_e4m3_encode(t) & 0x7F;
+      uint8_t codes[32];
+      if (s == 0) {
+        memset(codes, 0, 32);
+      } else {
+        float dec = (float)nvo_e4m3_value(s);
+        float d = dec * g;
+        for (int i = 0; i < 32; i++) {
+          float v = bf16_to_f32(blk[i]) / d;
+          codes[i] = (uint8_t)nvo_e2m1_encode(v);
+        }
+      }
+      for (int j = 0; j < 16; j++)
+        q[r * (K / 2) + c * 16 + j] = (uint8_t)(codes[2 * j] | (codes[2 * j + 1] << 4));
+      sf[sf_offset_bs(r, c, K, 32)] = (uint8_t)s;
+    }
+  }
+}
+
+/* Decoded logical row of a compressed sparse weight: zeros at pruned positions,
+ * kept element k = E2M1(stored code) * E4M3(scale of its 16-element stored block). */
+static void decode_sparse_row(const uint8_t* cq, const uint8_t* csf, const uint8_t* meta, int64_t n, int64_t K,
+                              double* out) {
+  const int64_t Ks = K / 2;
+  for (int64_t k = 0; k < K; k++) out[k] = 0.0;
+  for (int64_t g = 0; g < K / 8; g++) {
+    int nib = (meta[n * (K / 16) + g / 2] >> (4 * (g & 1))) & 15;
+    int pi[2] = {nib & 3, nib >> 2};
+    for (int h = 0; h < 2; h++)
+      for (int e = 0; e < 2; e++) {
+        int64_t st = 4 * g + 2 * h + e;                 /* stored index */
+        int64_t k = 8 * g + 2 * pi[h] + e;              /* its logical K position */
+        uint8_t byte = cq[n * (Ks / 2) + st / 2];
+        int code = (st & 1) ? (byte >> 4) : (byte & 15);
+        out[k] = nvo_e2m1_value(code) * nvo_e4m3_value(csf[sf_offset_bs(n, st / 16, Ks, 16)]);
+      }
+  }
+}
+
+/*
+ * Sparse GEMM: y[i, j] = (sum_k X^[rows[i], k] * W^[cols[j], k]) * gx * gw in float64, X^
+ * decoded with 32-element blocks (scales xsf), W^ the decoded logical weight (cq [N, K/4]
+ * bytes of compressed codes, csf its 16-element-block scales over K/2, meta [N, K/16]).
+ * absdot as in nvo_gemm_f64.
+ */
+void nvo_sparse_gemm_f64(const uint8_t* xq, const uint8_t* xsf, float gx, const uint8_t* cq, const uint8_t* csf,
+                         const uint8_t* meta, float gw, int64_t M, int64_t N, int64_t K, const int64_t* rows,
+                         int64_t nr, const int64_t* cols, int64_t nc, double* y, double* absdot) {
+  init_tables();
+  if (!rows) nr = M;
+  if (!cols) nc = N;
+  double* wd = (double*)malloc(sizeof(double) * (size_t)nc * (size_t)K);
+#pragma omp parallel for schedule(static)
+  for (int64_t j = 0; j < nc; j++) decode_sparse_row(cq, csf, meta, cols ? cols[j] : j, K, wd + j * K);
+#pragma omp parallel
+  {
+    double* xd = (double*)malloc(sizeof(double) * (size_t)K);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nr; i++) {
+      int64_t m = rows ? rows[i] : i;
+      for (int64_t k = 0; k < K; k++) {
+        uint8_t byte = xq[m * (K / 2) + k / 2];
+        int code = (k & 1) ? (byte >> 4) : (byte & 15);
+        xd[k] = nvo_e2m1_value(code) * nvo_e4m3_value(xsf[sf_offset_bs(m, k / 32, K, 32)]);
+      }
+      for (int64_t j = 0; j < nc; j++) {
+        double s = 0.0, sa = 0.0;
+        const double* wj = wd + j * K;
+        for (int64_t k = 0; k < K; k++) {
+          double p = xd[k] * wj[k];
+          s += p;
+          sa += fabs(p);
+        }
+        y[i * nc + j] = s * (double)gx * (double)gw;
+        if (absdot) absdot[i * nc + j] = sa * fabs((double)gx * (double)gw);
+      }
+    }
+    free(xd);
+  }
+  free(wd);
+}
+
 int nvo_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();
