@@ -197,6 +197,61 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, const float*
                               size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * Pair-wise 2:4 sparse NVFP4 ("FP4 structured sparsity", named as a kernel-level lever in
+ * "The Moment of Recalibration", magik.net, The Broader Narrative Arc; the pages give no
+ * format). The sparse block-scaled tensor-core MMA on FP4 keeps two of the four pairs of
+ * neighbouring K elements in every group of 8 (4:8 pair-wise), reads one index nibble per
+ * group and applies one scale per 32 K elements of each operand. Formats:
+ *   - compressed weights c [N, K/2]: the kept pairs of each group in increasing index order,
+ *     quantised as an ordinary NVFP4 tensor (nvfp4_amax + nvfp4_quantize over [N, K/2]:
+ *     codes [N, K/4] bytes, 16-element-block scales nvfp4_scale_bytes(N, K/2));
+ *   - metadata: per group the nibble i0 | i1 << 2 of the kept pair indices (i0 < i1), tiled
+ *     per 128 rows x 512 K elements into 4096-byte tiles, row r's 32 bytes (groups 2b in the
+ *     low nibble of byte b) at (r%128/8)*256 + (b/16)*128 + (r%8)*16 + b%16; padding zero;
+ *     nvfp4_sparse_meta_bytes(N, K) bytes;
+ *   - activations quantised with 32-element blocks (nvfp4_quantize_b32).
+ * K must be a multiple of 128.
+ */
+
+/* Bytes of the tiled metadata of an [N, K] weight. */
+int64_t nvfp4_sparse_meta_bytes(int64_t N, int64_t K);
+/* Bytes of a tiled scale tensor with 32-element blocks: ceil(rows/128)*128 * ceil(K/128)*4. */
+int64_t nvfp4_scale_bytes_b32(int64_t rows, int64_t K);
+
+/*
+ * Prunes and compresses a dense bf16 weight: in each group of 8 K elements the two pairs
+ * with the largest |w_2j| + |w_2j+1| (one fp32 addition; ties to the lower pair index)
+ * are kept. Bit-exact with the library's CPU oracle.
+ *   w         device bf16 [N, K] row-major, 16-byte aligned
+ *   c_out     device bf16 [N, K/2], written
+ *   meta_out  device u8, nvfp4_sparse_meta_bytes(N, K) bytes, tiled as above, written
+ */
+int nvfp4_prune_pairs(const uint16_t* w, int64_t N, int64_t K, uint16_t* c_out, uint8_t* meta_out, void* stream);
+
+/*
+ * nvfp4_quantize with 32-element blocks (the activation operand of nvfp4_sparse_gemm):
+ * s = E4M3_rn_satfinite((amax_32 / 6) / g), q = E2M1_rn_satfinite(x / (E4M3(s) * g)).
+ *   q_out   [M, K/2]; sf_out nvfp4_scale_bytes_b32(M, K) bytes (128 x 4 tiles over K/32)
+ * Bit-exact with the library's CPU oracle.
+ */
+int nvfp4_quantize_b32(const uint16_t* x, int64_t M, int64_t K, const float* global_scale, uint8_t* q_out,
+                       uint8_t* sf_out, void* stream);
+
+/*
+ * y = x @ W^T with W pair-wise 2:4 sparse, on the sparse tensor cores (tcgen05.mma.sp).
+ *   a, sfa, ga      x: packed [M, K/2], 32-element-block scales nvfp4_scale_bytes_b32(M, K)
+ *   b_c, sfb_c, gb  compressed W: codes [N, K/4], scales nvfp4_scale_bytes(N, K/2), global scale
+ *   meta            tiled metadata, nvfp4_sparse_meta_bytes(N, K) bytes
+ *   y               bf16 [M, N], written
+ * A weight-streaming kernel (the weights' bytes are 39 % fewer than dense NVFP4's); M above
+ * 128 runs as one launch per 128 rows. The result agrees with the oracle within
+ * |y - y_ref| <= 4e-3 |y_ref| + 1e-5 sum_k |x^_k w^_k|.
+ */
+int nvfp4_sparse_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b_c,
+                      const uint8_t* sfb_c, const uint8_t* meta, const float* gb, uint16_t* y, int64_t M, int64_t N,
+                      int64_t K, int32_t* dev_status, void* stream);
+
+/*
  * Allocation-free variant of nvfp4_grouped_gemm. The pages have no counterpart;
  * it exists for callers that cannot call cudaMalloc at the point where they run
  * the MoE layer: runtimes that hand kernels a fixed memory budget and offer no

@@ -42,7 +42,9 @@ EXPORTS = ["nvfp4_status_string", "nvfp4_scale_bytes", "nvfp4_amax_workspace_byt
            "nvfp4_grouped_gemm_swiglu",
            "nvfp4_grouped_gemm_noalloc",
            "nvfp4_encode_e2m1",
-           "nvfp4_encode_e4m3", "nvfp4_tune", "nvfp4_last_launch_count"]
+           "nvfp4_encode_e4m3", "nvfp4_tune", "nvfp4_last_launch_count",
+           "nvfp4_sparse_meta_bytes", "nvfp4_scale_bytes_b32", "nvfp4_prune_pairs", "nvfp4_quantize_b32",
+           "nvfp4_sparse_gemm"]
 
 
 class NVFP4Error(RuntimeError):
@@ -98,6 +100,13 @@ def lib():
             L.nvfp4_encode_e2m1.argtypes = [_vp, _i64, _vp, _vp]
             L.nvfp4_encode_e4m3.argtypes = [_vp, _i64, _vp, _vp]
             L.nvfp4_tune.argtypes = [ctypes.c_int, ctypes.c_int]
+            L.nvfp4_sparse_meta_bytes.restype = _i64
+            L.nvfp4_sparse_meta_bytes.argtypes = [_i64, _i64]
+            L.nvfp4_scale_bytes_b32.restype = _i64
+            L.nvfp4_scale_bytes_b32.argtypes = [_i64, _i64]
+            L.nvfp4_prune_pairs.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp]
+            L.nvfp4_quantize_b32.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _vp]
+            L.nvfp4_sparse_gemm.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]
             L.nvfp4_last_launch_count.restype = ctypes.c_int
             _lib = L
     return _lib
@@ -287,8 +296,8 @@ def nvfp4_grouped_gemm_noalloc(a, sfa, ga, b, sfb, gb, expert_offsets, E: int, M
                                K: int, y=None, dev_status=None, stream=None):
     """nvfp4_grouped_gemm without a workspace argument: the library's built-in scratch is used.
 
-    For callers that cannot allocate device memory where they run the MoE layer (for
-    example inside CUDA-graph capture). Only `y` is allocated here when not given.
+    For callers that cannot allocate device memory where they run the MoE layer (runtimes
+    with a fixed memory budget and no allocator). Only `y` is allocated here when not given.
     """
     for t, n in ((a, "a"), (sfa, "sfa"), (b, "b"), (sfb, "sfb")):
         _cuda(t, torch.uint8, n)
@@ -300,6 +309,55 @@ def nvfp4_grouped_gemm_noalloc(a, sfa, ga, b, sfb, gb, expert_offsets, E: int, M
            lib().nvfp4_grouped_gemm_noalloc(_ptr(a), _ptr(sfa), _ptr(ga), _ptr(b), _ptr(sfb), _ptr(gb),
                                             _ptr(expert_offsets), E, M_total, N, K, _ptr(y),
                                             _ptr(dev_status), _stream(stream)))
+    return y
+
+
+def nvfp4_sparse_meta_bytes(N: int, K: int) -> int:
+    return int(lib().nvfp4_sparse_meta_bytes(N, K))
+
+
+def nvfp4_scale_bytes_b32(rows: int, K: int) -> int:
+    return int(lib().nvfp4_scale_bytes_b32(rows, K))
+
+
+def nvfp4_prune_pairs(w: torch.Tensor, c_out=None, meta_out=None, stream=None):
+    """Pair-wise 2:4 pruning + compression of a bf16 weight [N, K]: returns (c bf16 [N, K/2],
+    tiled metadata uint8 [nvfp4_sparse_meta_bytes(N, K)])."""
+    _cuda(w, torch.bfloat16, "w")
+    N, K = w.shape
+    c_out = torch.empty((N, K // 2), dtype=torch.bfloat16, device=w.device) if c_out is None else c_out
+    meta_out = (torch.empty(nvfp4_sparse_meta_bytes(N, K), dtype=torch.uint8, device=w.device)
+                if meta_out is None else meta_out)
+    _check("nvfp4_prune_pairs", lib().nvfp4_prune_pairs(_ptr(w), N, K, _ptr(c_out), _ptr(meta_out),
+                                                        _stream(stream)))
+    return c_out, meta_out
+
+
+def nvfp4_quantize_b32(x: torch.Tensor, global_scale: torch.Tensor, q_out=None, sf_out=None, stream=None):
+    """bf16 [M, K] -> NVFP4 with 32-element blocks: (q u8 [M, K/2], sf u8 [nvfp4_scale_bytes_b32(M, K)])."""
+    _cuda(x, torch.bfloat16, "x")
+    _cuda(global_scale, torch.float32, "global_scale")
+    M, K = x.shape
+    q_out = torch.empty((M, K // 2), dtype=torch.uint8, device=x.device) if q_out is None else q_out
+    sf_out = (torch.empty(nvfp4_scale_bytes_b32(M, K), dtype=torch.uint8, device=x.device)
+              if sf_out is None else sf_out)
+    _check("nvfp4_quantize_b32", lib().nvfp4_quantize_b32(_ptr(x), M, K, _ptr(global_scale), _ptr(q_out),
+                                                          _ptr(sf_out), _stream(stream)))
+    return q_out, sf_out
+
+
+def nvfp4_sparse_gemm(a, sfa, ga, b_c, sfb_c, meta, gb, M: int, N: int, K: int, y=None, dev_status=None,
+                      stream=None):
+    """y = x @ W^T, W pair-wise 2:4 sparse (compressed codes b_c [N, K/4], scales sfb_c, tiled meta),
+    x in 32-element blocks; bf16 [M, N]."""
+    for t, n in ((a, "a"), (sfa, "sfa"), (b_c, "b_c"), (sfb_c, "sfb_c"), (meta, "meta")):
+        _cuda(t, torch.uint8, n)
+    _cuda(ga, torch.float32, "ga")
+    _cuda(gb, torch.float32, "gb")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=a.device) if y is None else y
+    _check("nvfp4_sparse_gemm", lib().nvfp4_sparse_gemm(_ptr(a), _ptr(sfa), _ptr(ga), _ptr(b_c), _ptr(sfb_c),
+                                                        _ptr(meta), _ptr(gb), _ptr(y), M, N, K, _ptr(dev_status),
+                                                        _stream(stream)))
     return y
 
 

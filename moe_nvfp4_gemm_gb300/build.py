@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libnvfp4.so")
-SOURCES = ["capi.cu", "quantize.cu", "gemm_dense.cu", "gemm_stream.cu"]
+SOURCES = ["capi.cu", "quantize.cu", "gemm_dense.cu", "gemm_stream.cu", "sparse.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -448,6 +448,130 @@ int nvfp4_gemm_quantize_out(const uint8_t* a, const uint8_t* sfa, const float* g
   return rc;
 }
 
+// ---- pair-wise 2:4 sparse weights ------------------------------------------------------------
+
+int64_t nvfp4_sparse_meta_bytes(int64_t N, int64_t K) {
+  if (N < 0 || K < 0) return 0;
+  return (N + 127) / 128 * ((K + 511) / 512) * 4096;
+}
+
+int64_t nvfp4_scale_bytes_b32(int64_t rows, int64_t K) {
+  if (rows < 0 || K < 0) return 0;
+  return (rows + 127) / 128 * 128 * ((K / 32 + 3) / 4 * 4);
+}
+
+int nvfp4_prune_pairs(const uint16_t* w, int64_t N, int64_t K, uint16_t* c_out, uint8_t* meta_out, void* stream) {
+  g_last_launches = 0;
+  if (N < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
+  if (K % 128 != 0 || N > kMaxDim || K > kMaxDim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (N == 0 || K == 0) return NVFP4_OK;
+  if (!w || !c_out || !meta_out) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(c_out)) return NVFP4_ERR_ALIGNMENT;
+  DevInfo d;
+  int rc = device_info(d);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // padding of the tiled metadata (rows up to a multiple of 128, K up to 512) reads as zero
+  if (N % 128 != 0 || K % 512 != 0) {
+    if ((rc = from_cuda(cudaMemsetAsync(meta_out, 0, static_cast<size_t>(nvfp4_sparse_meta_bytes(N, K)), st))))
+      return rc;
+  }
+  rc = from_cuda(launch_prune_pairs(w, N, K, c_out, meta_out, d.sms, st));
+  g_last_launches = 1;
+  return rc;
+}
+
+int nvfp4_quantize_b32(const uint16_t* x, int64_t M, int64_t K, const float* g, uint8_t* q, uint8_t* sf,
+                       void* stream) {
+  g_last_launches = 0;
+  if (M < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
+  if (K % 128 != 0 || M > kMaxDim || K > kMaxDim || (M + 127) / 128 > 65535) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0 || K == 0) return NVFP4_OK;
+  if (!x || !g || !q || !sf) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return NVFP4_ERR_ALIGNMENT;
+  DevInfo d;
+  int rc = device_info(d);
+  if (rc) return rc;
+  rc = from_cuda(launch_quantize_b32(x, M, K, g, q, sf, static_cast<cudaStream_t>(stream)));
+  g_last_launches = 1;
+  return rc;
+}
+
+int nvfp4_sparse_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b_c, const uint8_t* sfb_c,
+                      const uint8_t* meta, const float* gb, uint16_t* y, int64_t M, int64_t N, int64_t K,
+                      int32_t* dev_status, void* stream) {
+  g_last_launches = 0;
+  int rc = check_gemm_shape(M, N, K);
+  if (rc) return rc;
+  if (K % 128 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return NVFP4_OK;
+  if (!a || !sfa || !ga || !b_c || !sfb_c || !meta || !gb || !y) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(sfa) || !aligned16(b_c) || !aligned16(sfb_c) || !aligned16(meta) ||
+      !aligned16(y))
+    return NVFP4_ERR_ALIGNMENT;
+  DevInfo d;
+  rc = device_info(d);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // weight streaming (swap-AB): the compressed weights on the MMA's 128-lane side, up to 128
+  // token rows on its N side; larger M runs as one launch per 128-row chunk
+  CUtensorMap tmW;
+  if ((rc = encode_2d(&tmW, b_c, N, K / 4, 128))) return rc;
+  const int NT = static_cast<int>((N + 127) / 128);
+  const int KB = static_cast<int>((K + 511) / 512);
+  const int64_t chunk_sf = (K / 128) * 512;  // x scale bytes per 128 rows
+  int launches = 0;
+  for (int64_t m0 = 0; m0 < M; m0 += 128) {
+    const int Mc = static_cast<int>(M - m0 < 128 ? M - m0 : 128);
+    CUtensorMap tmX;
+    if ((rc = encode_2d(&tmX, a + m0 * (K / 2), Mc, K / 2, 16))) return rc;
+    StreamArgs s = {};
+    s.sfw = sfb_c;
+    s.sfx = sfa + (m0 / 128) * chunk_sf;
+    s.ga = ga;
+    s.gb = gb;
+    s.y = y + m0 * N;
+    s.status = dev_status;
+    s.M = Mc;
+    s.N = static_cast<int>(N);
+    s.K = static_cast<int>(K);
+    s.meta = meta;
+    s.x_rows = static_cast<int>(pad16(Mc));
+    s.acc_cols = (s.x_rows + 31) / 32 * 32;
+    s.acc_bufs = 1;
+    int split = g_tune.stream_split;
+    if (split == 0) {
+      split = (2 * d.sms) / NT;
+      split = split < 1 ? 1 : (split > 8 ? 8 : split);
+    }
+    if (split > KB) split = KB;
+    s.split = split;
+    s.pdl = stream_pdl_mode();
+    s.w_keep = g_tune.weight_l2;
+    s.watchdog_ns = watchdog_ns();
+    s.drop_stage = g_tune.withhold_stage;
+    const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0, true) - 1536;
+    const int recv_bytes = stream_recv_bytes(s.M, split);
+    int stages = g_tune.stream_stages;
+    if (stages == 0) {
+      stages = (110 * 1024 - 1536 - recv_bytes) / stage_bytes;  // two CTAs per SM
+      const int tmem_room = (256 - s.acc_cols) / 40;
+      if (stages > tmem_room) stages = tmem_room;
+      if (stages < 2) stages = 2;
+    }
+    while (split > 1 && stages * stage_bytes < recv_bytes) ++stages;
+    if (stream_smem_bytes(stages, s.x_rows, recv_bytes, true) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    s.stages = stages;
+    s.tmem_cols = pow2_at_least(s.acc_cols + 40 * stages);
+    if (s.tmem_cols > 512) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    rc = from_cuda(launch_stream(tmW, tmX, s, false, NT * split, st));
+    ++launches;
+    g_last_launches = launches;
+    if (rc) return rc;
+  }
+  return NVFP4_OK;
+}
+
 static int64_t grouped_max_tiles(int32_t E, int64_t M_total) { return (M_total + kGroupTileRows - 1) / kGroupTileRows + E; }
 
 static int64_t grouped_slab_offset(int32_t E, int64_t M_total) {

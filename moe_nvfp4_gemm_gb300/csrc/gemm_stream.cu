@@ -25,13 +25,18 @@
 namespace nvfp4 {
 
 
+// One ring stage: the 128-row weight tile (128 bytes a row), the token tile (one 128-byte
+// box a row; two for the sparse form, whose stage spans 512 K elements), the 2 KB of weight
+// and token scales, and for the sparse form the 4 KB metadata tile.
 struct StreamLayout {
-  int stage_bytes, x_off, sfw_off, sfx_off;
-  __host__ __device__ StreamLayout(int x_rows) {
+  int stage_bytes, x_off, xbox, sfw_off, sfx_off, meta_off;
+  __host__ __device__ StreamLayout(int x_rows, bool sparse = false) {
     x_off = 16384;
-    sfw_off = x_off + x_rows * 128;
+    xbox = x_rows * 128;
+    sfw_off = x_off + (sparse ? 2 : 1) * xbox;
     sfx_off = sfw_off + 2048;
-    stage_bytes = sfx_off + 2048;
+    meta_off = sfx_off + 2048;
+    stage_bytes = meta_off + (sparse ? 4096 : 0);
   }
 };
 
@@ -86,15 +91,21 @@ constexpr int kStreamWaiterWarp = 6;
 constexpr uint32_t kStreamHandoffBarrier = 1;
 constexpr uint32_t kStreamEpilogueBarrier = 2;  // the 4 epilogue warps
 
-// VARIANT (grouped only): bit 0 SwiGLU epilogue, bit 1 token gather in the load stage;
-// compiled separately so that the plain grouped kernel carries neither.
+// VARIANT: bit 0 SwiGLU epilogue, bit 1 token gather in the load stage (grouped only);
+// bit 2 pair-wise 2:4 sparse weights (dense path only): the weight tile holds compressed
+// values, a stage spans 512 K elements (four K = 128 sparse MMAs) and carries the metadata
+// tile. Compiled separately so that the plain kernels carry none of them.
 template <bool GROUPED, int VARIANT = 0>
 __global__ void __launch_bounds__(kStreamThreads, 2)
     k_gemm_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                   const StreamArgs p) {
+  constexpr bool SPARSE = (VARIANT & 4) != 0;
+  constexpr int KSTAGE = SPARSE ? 512 : 256;  // K elements per stage
+  constexpr int KMMA = KSTAGE / 4;            // K elements per MMA
+  constexpr int SF_COLS = SPARSE ? 40 : 32;   // TMEM columns per stage: scales (+ metadata)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const StreamLayout L(p.x_rows);
+  const StreamLayout L(p.x_rows, SPARSE);
   const int STAGES = p.stages;
   // Split-K (dense, S = p.split > 1): CTA rank r of a cluster owns tokens
   // [r * m_own, (r + 1) * m_own). Its partial sums leave from `part` = [token][128 rows]
@@ -122,8 +133,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   const uint64_t wd = p.watchdog_ns;
   const int N = p.N, K = p.K;
   const int NT = (N + 127) / 128;
-  const int KB = (K + 255) / 256;
-  const int64_t KC4 = K / 64;
+  const int KB = (K + KSTAGE - 1) / KSTAGE;
+  // 512-byte scale tiles per 128 rows: one per MMA step (weights over stored values)
+  const int64_t KC4 = K / KMMA;
+  const int64_t KMC = (K + 511) / 512;  // sparse: 4 KB metadata tiles per 128 weight rows
 
   // Where an item's tiles come from (computed once per item).
   struct Src {
@@ -131,6 +144,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     int n16;
     const uint8_t* sfw;
     const uint8_t* sfx;
+    const uint8_t* meta;
   };
   auto item_src = [&](const Item& it) {
     Src r;
@@ -139,7 +153,26 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     r.n16 = (it.rows + 15) >> 4;
     r.sfw = p.sfw + it.e * p.sfw_stride + static_cast<int64_t>(it.wt) * KC4 * 512;
     r.sfx = p.sfx + static_cast<int64_t>(it.slab) * KC4 * 512;
+    r.meta = SPARSE ? p.meta + static_cast<int64_t>(it.wt) * KMC * 4096 : nullptr;
     return r;
+  };
+  // The token tiles and their scales of stage st_idx = K block kb (sparse: two boxes per row).
+  auto issue_x = [&](uint8_t* st, uint64_t* bar, int kb, const Src& src, bool hint, uint64_t pol_x) {
+    const int nsub = min(4, (K - kb * KSTAGE) / KMMA);
+#pragma unroll
+    for (int bx = 0; bx < (SPARSE ? 2 : 1); ++bx)
+      for (int j = 0; j < src.n16; ++j) {
+        uint8_t* dst = st + L.x_off + bx * L.xbox + j * 2048;
+        const int32_t kx = kb * (KSTAGE / 2) + bx * 128;
+        if (hint)
+          tma_load_2d(dst, &tmX, bar, kx, src.row0 + j * 16, pol_x);
+        else
+          tma_load_2d_plain(dst, &tmX, bar, kx, src.row0 + j * 16);
+      }
+    if (hint)
+      bulk_load(st + L.sfx_off, src.sfx + kb * 2048, nsub * 512, bar, pol_x);
+    else
+      bulk_load_plain(st + L.sfx_off, src.sfx + kb * 2048, nsub * 512, bar);
   };
   // Requests stage st_idx = K block kb of an item: the 128-row weight tile and its
   // scales, and unless deferred (with_x false) the token tile and its scales.
@@ -149,35 +182,30 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     const int32_t wrow0 = src.wrow0;
     const uint8_t* sfw = src.sfw;
     const uint8_t* sfx = src.sfx;
-    const int nsub = min(4, (K - kb * 256) / 64);
+    const int nsub = min(4, (K - kb * KSTAGE) / KMMA);
     uint8_t* st = smem + st_idx * L.stage_bytes;
     uint64_t* bar = &full[st_idx];
-    mbar_arrive_expect_tx(bar, 16384 + n16 * 2048 + nsub * 1024);
+    mbar_arrive_expect_tx(bar, 16384 + (SPARSE ? 2 : 1) * n16 * 2048 + nsub * 1024 + (SPARSE ? 4096 : 0));
     if (hint) {
       tma_load_2d(st, &tmW, bar, kb * 128, wrow0, pol_w);
       bulk_load(st + L.sfw_off, sfw + kb * 2048, nsub * 512, bar, pol_w);
+      if (SPARSE) bulk_load(st + L.meta_off, src.meta + kb * 4096, 4096, bar, pol_w);
     } else {
       tma_load_2d_plain(st, &tmW, bar, kb * 128, wrow0);
       bulk_load_plain(st + L.sfw_off, sfw + kb * 2048, nsub * 512, bar);
+      if (SPARSE) bulk_load_plain(st + L.meta_off, src.meta + kb * 4096, 4096, bar);
     }
     if (with_x && GROUPED && (VARIANT & 2)) {
       // token gather: four rows per instruction from the one-row-box map of x
       for (int j = 0; j < n16 * 4; ++j)
         tma_gather4(st + L.x_off + j * 512, &tmX, bar, kb * 128, tok_idx[4 * j], tok_idx[4 * j + 1],
                     tok_idx[4 * j + 2], tok_idx[4 * j + 3]);
-    } else if (with_x) {
-      for (int j = 0; j < n16; ++j) {
-        if (hint)
-          tma_load_2d(st + L.x_off + j * 2048, &tmX, bar, kb * 128, src.row0 + j * 16, pol_x);
-        else
-          tma_load_2d_plain(st + L.x_off + j * 2048, &tmX, bar, kb * 128, src.row0 + j * 16);
-      }
-    }
-    if (with_x) {
       if (hint)
         bulk_load(st + L.sfx_off, sfx + kb * 2048, nsub * 512, bar, pol_x);
       else
         bulk_load_plain(st + L.sfx_off, sfx + kb * 2048, nsub * 512, bar);
+    } else if (with_x) {
+      issue_x(st, bar, kb, src, hint, pol_x);
     }
   };
   // Dense path: the first ring of this CTA's (single) item is requested by thread 0
@@ -315,14 +343,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         if (pending && (npend == STAGES || kb + 1 == it.kb1)) {
           griddep_wait();
           if (elect_one()) {
-            for (int j = 0; j < npend; ++j) {
-              const int kbj = pend_kb[j];
-              const int nsub = min(4, (K - kbj * 256) / 64);
-              uint8_t* st = smem + pend_stage[j] * L.stage_bytes;
-              for (int r = 0; r < n16; ++r)
-                tma_load_2d_plain(st + L.x_off + r * 2048, &tmX, &full[pend_stage[j]], kbj * 128, it.row0 + r * 16);
-              bulk_load_plain(st + L.sfx_off, sfx + kbj * 2048, nsub * 512, &full[pend_stage[j]]);
-            }
+            for (int j = 0; j < npend; ++j)
+              issue_x(smem + pend_stage[j] * L.stage_bytes, &full[pend_stage[j]], pend_kb[j], src, false, 0);
           }
           __syncwarp();
           pending = false;
@@ -365,7 +387,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     Item it;
     for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it); i += stride) {
       const int n_mma = ((it.rows + 15) >> 4) * 16;
-      const uint32_t idesc = idesc_nvf4(128, n_mma);
+      const uint32_t idesc = SPARSE ? idesc_nvf4_sp(128, n_mma) : idesc_nvf4(128, n_mma);
       const uint32_t acc = tmem + buf * p.acc_cols;
       bool item_ok = true;
       for (int kb = it.kb0; kb < it.kb1; ++kb) {
@@ -376,22 +398,32 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
           if (elect_one()) {
             // Fully unrolled: a data-dependent trip count here makes the elected lane
             // issue each tcgen05 instruction on its own, far more slowly.
-            const int nsub = min(4, (K - kb * 256) / 64);
+            const int nsub = min(4, (K - kb * KSTAGE) / KMMA);
             const uint32_t w_addr = smem_u32(smem + s * L.stage_bytes);
             const uint32_t x_addr = w_addr + L.x_off;
-            const uint32_t sf_col = sf_base + s * 32;
+            const uint32_t sf_col = sf_base + s * SF_COLS;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               if (kk < nsub) {
                 tc_cp_32x128b_x4(sf_col + kk * 4, desc_sf(w_addr + L.sfw_off + kk * 512));
                 tc_cp_32x128b_x4(sf_col + 16 + kk * 4, desc_sf(w_addr + L.sfx_off + kk * 512));
               }
+            if (SPARSE) tc_cp_128x256b(sf_col + 32, w_addr + L.meta_off);  // 8 columns: 2 per MMA
             const uint64_t wdesc = desc_sw128(w_addr), xdesc = desc_sw128(x_addr);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              if (kk < nsub)
-                tc_mma_nvf4(acc, wdesc + 2 * kk, xdesc + 2 * kk, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4,
-                            (kb != it.kb0) || (kk != 0));
+              if (kk < nsub) {
+                if (SPARSE) {
+                  // 32 stored bytes of each weight row per MMA; the token rows' 64 bytes (128 K
+                  // elements) at offset 0 or 64 of box kk / 2
+                  const uint64_t xd = desc_sw128(x_addr + (kk >> 1) * L.xbox) + (kk & 1) * 4;
+                  tc_mma_nvf4_sp(acc, wdesc + 2 * kk, xd, idesc, sf_col + 32 + 2 * kk, sf_col + kk * 4,
+                                 sf_col + 16 + kk * 4, (kb != it.kb0) || (kk != 0));
+                } else {
+                  tc_mma_nvf4(acc, wdesc + 2 * kk, xdesc + 2 * kk, idesc, sf_col + kk * 4, sf_col + 16 + kk * 4,
+                              (kb != it.kb0) || (kk != 0));
+                }
+              }
             tc_commit(&empty[s]);
           }
           __syncwarp();
@@ -673,7 +705,8 @@ template <bool GROUPED, int VARIANT>
 static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, int grid,
                                    cudaStream_t st) {
   // grouped: 256 bytes of token indices (the token gather); dense: the reduction's receive area
-  const int smem = stream_smem_bytes(a.stages, a.x_rows, GROUPED ? 256 : stream_recv_bytes(a.M, a.split));
+  const int smem = stream_smem_bytes(a.stages, a.x_rows, GROUPED ? 256 : stream_recv_bytes(a.M, a.split),
+                                     (VARIANT & 4) != 0);
   cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_gemm_stream<GROUPED, VARIANT>));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -705,13 +738,13 @@ static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tm
 // Receive area of the one-way split-K reduction: S slots of ceil(M / S) tokens x 128 fp32.
 int stream_recv_bytes(int M, int split) { return split > 1 ? split * ((M + split - 1) / split) * 512 : 0; }
 
-int stream_smem_bytes(int stages, int x_rows, int recv_bytes) {
-  return stages * StreamLayout(x_rows).stage_bytes + recv_bytes + 1024 + 512;
+int stream_smem_bytes(int stages, int x_rows, int recv_bytes, bool sparse) {
+  return stages * StreamLayout(x_rows, sparse).stage_bytes + recv_bytes + 1024 + 512;
 }
 
 cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, bool grouped, int grid,
                           cudaStream_t st) {
-  if (!grouped) return launch_stream_t<false, 0>(tmW, tmX, a, grid, st);
+  if (!grouped) return a.meta ? launch_stream_t<false, 4>(tmW, tmX, a, grid, st) : launch_stream_t<false, 0>(tmW, tmX, a, grid, st);
   if (a.row_token && a.swiglu) return cudaErrorInvalidValue;  // no entry point combines them
   if (a.row_token) return launch_stream_t<true, 2>(tmW, tmX, a, grid, st);
   if (a.swiglu) return launch_stream_t<true, 1>(tmW, tmX, a, grid, st);

@@ -70,6 +70,7 @@ struct StreamArgs {
   int w_keep;                // weights loaded L2 evict_last (kept resident across calls), else evict_first
   uint64_t watchdog_ns;      // limit of every pipeline wait
   int drop_stage;            // test hook: k >= 1 withholds the k-th stage CTA 0 loads (0: none)
+  const uint8_t* meta;       // dense path, pair-wise 2:4 sparse weights: tiled metadata (null: dense)
 };
 
 
@@ -80,6 +81,10 @@ cudaError_t launch_amax(const uint16_t* x, int64_t n, float* amax_out, float* g_
 cudaError_t launch_quantize(const uint16_t* x, int64_t M, int64_t K, const float* g, uint8_t* q, uint8_t* sf,
                             cudaStream_t st);
 cudaError_t launch_encode(int which, const float* v, int64_t n, uint8_t* out, cudaStream_t st);
+cudaError_t launch_prune_pairs(const uint16_t* w, int64_t N, int64_t K, uint16_t* c, uint8_t* meta, int sms,
+                               cudaStream_t st);
+cudaError_t launch_quantize_b32(const uint16_t* x, int64_t M, int64_t K, const float* g, uint8_t* q, uint8_t* sf,
+                                cudaStream_t st);
 cudaError_t launch_dense(const CUtensorMap& tmA, const CUtensorMap& tmB, const DenseArgs& a, int bn, int grid,
                          cudaStream_t st);
 cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
@@ -91,7 +96,7 @@ cudaError_t launch_grouped_prep(const int32_t* offsets, const int32_t* row_token
                                 const uint8_t* sfx,
                                 int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
                                 cudaStream_t st, const uint8_t* x_tok = nullptr, uint8_t* xg = nullptr);
-int stream_smem_bytes(int stages, int x_rows, int recv_bytes);
+int stream_smem_bytes(int stages, int x_rows, int recv_bytes, bool sparse = false);
 int stream_recv_bytes(int M, int split);
 
 // Raises `func`'s dynamic shared-memory limit to the opt-in maximum, once per

@@ -107,16 +107,25 @@ DEVI float div_rn_by(float x, float d, float y) {
   return __fmaf_rn(__fmaf_rn(-q1, d, x), y, q1);
 }
 
-// g_inv = RN(1 / g), computed once per thread.
-DEVI void quantize_block(const uint32_t (&w)[8], float g, float g_inv, uint32_t& s, uint2& packed_out) {
+// Largest |x| of 16 bf16 values (8 packed pairs), exact.
+DEVI float block_amax16(const uint32_t (&w)[8]) {
   // |x| of both halves at once (sign bits cleared), maximum on the bf16 pairs (exact)
   uint32_t m2 = w[0] & 0x7FFF7FFFu;
 #pragma unroll
   for (int j = 1; j < 8; ++j) asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(w[j] & 0x7FFF7FFFu));
-  const float amax = fmaxf(bf16lo(m2), bf16hi(m2));
-  // RN(RN(amax / 6) / g); 0x3e2aaaab = RN(1 / 6)
+  return fmaxf(bf16lo(m2), bf16hi(m2));
+}
+
+// E4M3 code of a block with maximum |x| amax: E4M3_rn_sat(RN(RN(amax / 6) / g)); g_inv = RN(1 / g).
+DEVI uint32_t block_scale_code(float amax, float g, float g_inv) {
+  // 0x3e2aaaab = RN(1 / 6)
   const float t = amax == 0.0f ? 0.0f : div_rn_by(div_rn_by(amax, 6.0f, __uint_as_float(0x3e2aaaabu)), g, g_inv);
-  s = e4m3_encode(t);
+  return e4m3_encode(t);
+}
+
+// E2M1 codes of 16 bf16 values (8 packed pairs) with block scale code s (0: all codes 0);
+// amax is the largest |x| of the block the scale belongs to (it bounds the quotients).
+DEVI uint2 block_codes16(const uint32_t (&w)[8], uint32_t s, float g, float amax) {
   uint32_t packed[2] = {0u, 0u};
   if (s != 0) {
     const float d = __fmul_rn(e4m3_decode(s), g);
@@ -151,7 +160,25 @@ DEVI void quantize_block(const uint32_t (&w)[8], float g, float g_inv, uint32_t&
       packed[h] = e2m1x8_encode(v);
     }
   }
-  packed_out = make_uint2(packed[0], packed[1]);
+  return make_uint2(packed[0], packed[1]);
+}
+
+// One 16-element block: scale code s and 8 bytes of packed codes. g_inv = RN(1 / g),
+// computed once per thread.
+DEVI void quantize_block(const uint32_t (&w)[8], float g, float g_inv, uint32_t& s, uint2& packed_out) {
+  const float amax = block_amax16(w);
+  s = block_scale_code(amax, g, g_inv);
+  packed_out = block_codes16(w, s, g, amax);
+}
+
+// One 32-element block (the dense operand of the pair-wise sparse GEMM): one scale from the
+// amax of all 32 values, then the codes of both halves with it.
+DEVI void quantize_block32(const uint32_t (&w0)[8], const uint32_t (&w1)[8], float g, float g_inv, uint32_t& s,
+                           uint2& p0, uint2& p1) {
+  const float amax = fmaxf(block_amax16(w0), block_amax16(w1));
+  s = block_scale_code(amax, g, g_inv);
+  p0 = block_codes16(w0, s, g, amax);
+  p1 = block_codes16(w1, s, g, amax);
 }
 
 }  // namespace nvfp4

@@ -295,6 +295,33 @@ DEVI void tc_mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_
       : "memory");
 }
 
+// D(tmem) (+)= A(smem) * B(smem)^T with A pair-wise 2:4 sparse (4:8 on FP4): K = 128 per
+// instruction, A holds 64 kept values a row; `meta_tmem` holds each row's 16 index nibbles
+// (lane = row, two columns, group g at nibble g % 8 of column g / 8); one UE4M3 scale per 32
+// K elements of each operand (4 per row, the same TMEM tiles as a dense K = 64 step).
+DEVI void tc_mma_nvf4_sp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t meta_tmem,
+                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\t"
+      "tcgen05.mma.sp.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, [%3], %4, [%5], [%6], p;\n\t"
+      "}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(meta_tmem), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// 128 rows x 32 bytes from shared memory into TMEM lanes 0-127, columns [col, col+8).
+// Source layout: rows in groups of 8, each row's 32 bytes as two 16-byte halves,
+// (r/8)*256 + (half)*128 + (r%8)*16 (no swizzle; leading offset 128, stride 256).
+DEVI void tc_cp_128x256b(uint32_t taddr, uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>(128 >> 4) << 16;
+  d |= static_cast<uint64_t>(256 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns.
 DEVI void tmem_ld32(uint32_t taddr, uint32_t* r) {
   asm volatile(
@@ -378,6 +405,9 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
   return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
+
+// The same with the sparsity flag (bit 2): A pair-wise sparse, shape M x N x 128.
+__host__ __device__ constexpr uint32_t idesc_nvf4_sp(int M, int N) { return idesc_nvf4(M, N) | (1u << 2); }
 
 DEVI uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

@@ -106,3 +106,24 @@ def test_tune_rejects_bad_values(lib):
     assert lib.nvfp4_tune(10, -1) == -1
     assert lib.nvfp4_tune(10, 1) == 0
     assert lib.nvfp4_tune(10, 0) == 0
+
+
+def test_sparse_sizes_match_oracle(lib):
+    for rows, K in [(1, 128), (128, 512), (130, 8192), (4096, 6144), (0, 128)]:
+        assert lib.nvfp4_scale_bytes_b32(rows, K) == oracle.scale_bytes_b32(rows, K)
+        assert lib.nvfp4_sparse_meta_bytes(rows, K) == oracle.meta_tiled_bytes(rows, K)
+    assert lib.nvfp4_sparse_meta_bytes(-1, 128) == 0 and lib.nvfp4_scale_bytes_b32(4, -1) == 0
+
+
+def test_sparse_host_validation(lib):
+    sg = lambda M, N, K, a=16, meta=16: lib.nvfp4_sparse_gemm(P(a), P(16), P(16), P(16), P(16), P(meta), P(16),
+                                                              P(16), M, N, K, None, None)
+    assert sg(0, 128, 256) == 0                  # empty M
+    assert sg(4, 128, 192) == -2                 # K % 128
+    assert sg(4, 12, 256) == -2                  # N % 8
+    assert sg(4, 128, 256, meta=0) == -1         # null metadata
+    assert sg(4, 128, 256, a=24) == -3           # misaligned operand
+    pr = lambda N, K, w=16: lib.nvfp4_prune_pairs(P(w), N, K, P(16), P(16), None)
+    assert pr(0, 128) == 0 and pr(4, 64) == -2 and pr(4, 128, w=0) == -1 and pr(4, 128, w=8) == -3
+    qb = lambda M, K, x=16: lib.nvfp4_quantize_b32(P(x), M, K, P(16), P(16), P(16), None)
+    assert qb(0, 128) == 0 and qb(4, 64) == -2 and qb(4, 128, x=0) == -1 and qb(4, 128, x=24) == -3
