@@ -43,7 +43,8 @@ def _timed_out_then_recovers(run, check, stage):
 
 
 # (kernel selection, M): the single-CTA tile kernel, the CTA-pair kernel, the weight-streaming
-# kernel alone and in split-K clusters of 4 (whose owners wait for every peer's partials)
+# kernel alone and in split-K clusters of 4 (whose owners wait for every peer's partials);
+# the sparse variant of the streaming kernel and the grouped kernel below
 DENSE_FAMILIES = {
     "tile_single_cta": (dict(STREAM_MAX_M=-1, DENSE_KERNEL=1), 256),
     "tile_cta_pair": (dict(STREAM_MAX_M=-1, DENSE_KERNEL=2), 256),
@@ -64,6 +65,14 @@ def test_dense_kernels_time_out_cleanly_and_recover(family, stage):
         return m.nvfp4_gemm(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, M, 512, 2048, dev_status=st)
 
     _timed_out_then_recovers(run, lambda y: check_gemm(y, A, B), stage)
+
+
+@pytest.mark.parametrize("stage", [1, 2])
+def test_sparse_kernel_times_out_cleanly_and_recovers(stage):
+    from tests.test_gpu_sparse import Sparse
+    g = Sparse(16, 256, 4096, 44)
+    m.nvfp4_tune(m.NVFP4_TUNE_STREAM_SPLIT, 4)
+    _timed_out_then_recovers(lambda st: g.run(status=st), g.check, stage)
 
 
 @pytest.mark.parametrize("stage", [1, 3])
