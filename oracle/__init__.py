@@ -415,5 +415,27 @@ def sparse_gemm(xq, xsf, gx, cq, csf, meta, gw, M: int, N: int, K: int, rows=Non
     return y, ad
 
 
+def grouped_sparse_gemm(xq, xsf, gx, cq, csf, meta, gw, offsets, E: int, M_total: int, N: int, K: int,
+                        rows=None, cols=None):
+    """Grouped (MoE) form of sparse_gemm: rows offsets[e] .. offsets[e+1]-1 of x (32-element
+    blocks, sorted by expert) use expert e's compressed weight cq[e], csf[e], meta[e] (linear
+    [N, K/16]) and global scale gw[e]. Returns (y, absdot) over the selected rows/cols."""
+    off = np.asarray(offsets, dtype=np.int64)
+    if off[0] != 0 or off[-1] != M_total or np.any(np.diff(off) < 0):
+        raise ValueError("malformed expert offsets")
+    sel = np.arange(M_total) if rows is None else np.asarray(rows, dtype=np.int64)
+    nc = N if cols is None else len(cols)
+    y = np.zeros((len(sel), nc), dtype=np.float64)
+    ad = np.zeros((len(sel), nc), dtype=np.float64)
+    for e in range(E):
+        pick = np.nonzero((sel >= off[e]) & (sel < off[e + 1]))[0]
+        if pick.size == 0:
+            continue
+        ye, ade = sparse_gemm(xq, xsf, gx, cq[e], csf[e], meta[e], gw[e], M_total, N, K, rows=sel[pick], cols=cols)
+        y[pick] = ye
+        ad[pick] = ade
+    return y, ad
+
+
 def num_threads() -> int:
     return int(lib().nvo_num_threads())

@@ -173,3 +173,30 @@ def test_sparse_gemm_exact_on_a_tiny_case():
                 total += xv[8 * g + 2 * pairs[h] + e] * wv
     expect = total * Fraction(float(gx)) * Fraction(float(gw))
     assert abs(Fraction(float(y[0, 0])) - expect) <= abs(expect) * Fraction(1, 2 ** 50)
+
+
+def test_grouped_sparse_gemm_is_per_expert_sparse_gemm_and_matches_dense_grouped():
+    E, N, K = 4, 40, 512
+    counts = np.array([5, 0, 17, 3])
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    Mt = int(off[-1])
+    xq, xsf, gx = oracle.quantize_b32(synth.normal_bf16((Mt, K), 81, 1.0, 1e-2))
+    ws = [oracle.sparse_quantize_weight(synth.moe_expert_weight(e, N, K, 82)) for e in range(E)]
+    cq = np.stack([w[0] for w in ws])
+    csf = np.stack([w[1] for w in ws])
+    gw = np.array([w[2] for w in ws], np.float32)
+    meta = np.stack([w[3] for w in ws])
+    y, ad = oracle.grouped_sparse_gemm(xq, xsf, gx, cq, csf, meta, gw, off, E, Mt, N, K)
+    for e in range(E):
+        r = np.arange(off[e], off[e + 1])
+        if r.size:
+            ye, _ = oracle.sparse_gemm(xq, xsf, gx, cq[e], csf[e], meta[e], gw[e], Mt, N, K, rows=r)
+            assert np.array_equal(y[r], ye)
+    # the dense grouped oracle on operands decompressed here
+    dq, dsf = zip(*[_decompress(cq[e], csf[e], meta[e], N, K) for e in range(E)])
+    x16 = oracle.sf_swizzle(np.repeat(oracle.sf_unswizzle_bs(xsf, Mt, K, 32), 2, axis=1), Mt, K)
+    yd, add = oracle.grouped_gemm(xq, x16, gx, np.stack(dq), np.stack(dsf), gw, off, E, Mt, N, K)
+    assert np.array_equal(y, yd) and np.array_equal(ad, add)
+    ys, _ = oracle.grouped_sparse_gemm(xq, xsf, gx, cq, csf, meta, gw, off, E, Mt, N, K, rows=[24, 0, 6],
+                                       cols=[39, 1])
+    assert np.array_equal(ys, y[np.ix_([24, 0, 6], [39, 1])])
