@@ -252,6 +252,22 @@ int nvfp4_sparse_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, con
                       int64_t K, int32_t* dev_status, void* stream);
 
 /*
+ * Grouped (MoE) form of nvfp4_sparse_gemm: rows expert_offsets[e] .. expert_offsets[e+1]-1
+ * of x (sorted by expert, quantised with nvfp4_quantize_b32 over the M_total rows) use
+ * expert e's pair-wise 2:4 sparse weight. Experts with no rows read none of their bytes.
+ *   b_c, sfb_c, gb   compressed experts: codes [E, N, K/4]; scales [E] x nvfp4_scale_bytes(N, K/2)
+ *                    bytes back to back; gb device fp32 [E]
+ *   meta             [E] x nvfp4_sparse_meta_bytes(N, K) bytes of tiled metadata, back to back
+ *   workspace        nvfp4_grouped_gemm_workspace_bytes(E, M_total, N, K) bytes, 256-byte aligned
+ * Other arguments and the device-side offset checks as nvfp4_grouped_gemm; K % 128 == 0.
+ */
+int nvfp4_grouped_sparse_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b_c,
+                              const uint8_t* sfb_c, const uint8_t* meta, const float* gb,
+                              const int32_t* expert_offsets, int32_t E, int64_t M_total, int64_t N, int64_t K,
+                              uint16_t* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              void* stream);
+
+/*
  * Allocation-free variant of nvfp4_grouped_gemm. The pages have no counterpart;
  * it exists for callers that cannot call cudaMalloc at the point where they run
  * the MoE layer: runtimes that hand kernels a fixed memory budget and offer no

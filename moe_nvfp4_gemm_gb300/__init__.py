@@ -44,7 +44,7 @@ EXPORTS = ["nvfp4_status_string", "nvfp4_scale_bytes", "nvfp4_amax_workspace_byt
            "nvfp4_encode_e2m1",
            "nvfp4_encode_e4m3", "nvfp4_tune", "nvfp4_last_launch_count",
            "nvfp4_sparse_meta_bytes", "nvfp4_scale_bytes_b32", "nvfp4_prune_pairs", "nvfp4_quantize_b32",
-           "nvfp4_sparse_gemm"]
+           "nvfp4_sparse_gemm", "nvfp4_grouped_sparse_gemm"]
 
 
 class NVFP4Error(RuntimeError):
@@ -107,6 +107,8 @@ def lib():
             L.nvfp4_prune_pairs.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp]
             L.nvfp4_quantize_b32.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _vp]
             L.nvfp4_sparse_gemm.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]
+            L.nvfp4_grouped_sparse_gemm.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64,
+                                                    _i64, _vp, _vp, _sz, _vp, _vp]
             L.nvfp4_last_launch_count.restype = ctypes.c_int
             _lib = L
     return _lib
@@ -358,6 +360,25 @@ def nvfp4_sparse_gemm(a, sfa, ga, b_c, sfb_c, meta, gb, M: int, N: int, K: int, 
     _check("nvfp4_sparse_gemm", lib().nvfp4_sparse_gemm(_ptr(a), _ptr(sfa), _ptr(ga), _ptr(b_c), _ptr(sfb_c),
                                                         _ptr(meta), _ptr(gb), _ptr(y), M, N, K, _ptr(dev_status),
                                                         _stream(stream)))
+    return y
+
+
+def nvfp4_grouped_sparse_gemm(a, sfa, ga, b_c, sfb_c, meta, gb, expert_offsets, E: int, M_total: int, N: int,
+                              K: int, y=None, workspace=None, dev_status=None, stream=None):
+    """Grouped form of nvfp4_sparse_gemm over pair-wise 2:4 sparse experts; bf16 [M_total, N]."""
+    for t, n in ((a, "a"), (sfa, "sfa"), (b_c, "b_c"), (sfb_c, "sfb_c"), (meta, "meta")):
+        _cuda(t, torch.uint8, n)
+    _cuda(ga, torch.float32, "ga")
+    _cuda(gb, torch.float32, "gb")
+    _cuda(expert_offsets, torch.int32, "expert_offsets")
+    y = torch.empty((M_total, N), dtype=torch.bfloat16, device=a.device) if y is None else y
+    if workspace is None:
+        workspace = torch.empty(max(1, nvfp4_grouped_gemm_workspace_bytes(E, M_total, N, K)), dtype=torch.uint8,
+                                device=a.device)
+    _check("nvfp4_grouped_sparse_gemm",
+           lib().nvfp4_grouped_sparse_gemm(_ptr(a), _ptr(sfa), _ptr(ga), _ptr(b_c), _ptr(sfb_c), _ptr(meta),
+                                           _ptr(gb), _ptr(expert_offsets), E, M_total, N, K, _ptr(y),
+                                           _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream)))
     return y
 
 

@@ -596,11 +596,16 @@ size_t nvfp4_grouped_gemm_gather_workspace_bytes(int32_t E, int64_t M_total, int
 }
 
 // row_token (null: none): routed row r reads row row_token[r] of the T-row activations a.
+// meta (null: dense weights): pair-wise 2:4 sparse experts, b / sfb their compressed codes and
+// scales, a / sfa the routed rows in 32-element blocks.
 static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b, const uint8_t* sfb,
                         const float* gb, const int32_t* expert_offsets, int32_t E, int64_t M_total, int64_t N,
                         int64_t K, uint16_t* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                        void* stream, int swiglu, const int32_t* row_token = nullptr, int64_t T = 0) {
+                        void* stream, int swiglu, const int32_t* row_token = nullptr, int64_t T = 0,
+                        const uint8_t* meta = nullptr) {
   g_last_launches = 0;
+  const bool sparse = meta != nullptr;
+  if (sparse && K % 128 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (row_token && M_total > 0 && (T <= 0 || T > kMaxDim)) return NVFP4_ERR_INVALID_ARG;
   if (E <= 0) return NVFP4_ERR_INVALID_ARG;
   int rc = check_gemm_shape(M_total, N, K);
@@ -636,13 +641,13 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   int prep_grid = static_cast<int>(prep_blocks < 4 * d.sms ? prep_blocks : 4 * d.sms);
   if (prep_grid < 1) prep_grid = 1;
   rc = from_cuda(launch_grouped_prep(expert_offsets, row_token, static_cast<int>(T), E, static_cast<int>(M_total),
-                                     static_cast<int>(K), sfa, n_tiles,
+                                     static_cast<int>(K), static_cast<int>(sparse ? K / 128 : K / 64), sfa, n_tiles,
                                      tiles, slabs, dev_status, prep_grid, st, xg ? a : nullptr, xg));
   g_last_launches = 1;
   if (rc) return rc;
 
   CUtensorMap tmW, tmX;
-  if ((rc = encode_2d(&tmW, b, static_cast<uint64_t>(E) * N, K / 2, 128))) return rc;
+  if ((rc = encode_2d(&tmW, b, static_cast<uint64_t>(E) * N, sparse ? K / 4 : K / 2, 128))) return rc;
   if (xg) {
     if ((rc = encode_2d(&tmX, xg, M_total, K / 2, 16))) return rc;
     row_token = nullptr;  // the GEMM reads the copied rows
@@ -655,7 +660,9 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   s.row_token = row_token;
   s.T = static_cast<int>(T);
   s.sfw = sfb;
-  s.sfw_stride = nvfp4_scale_bytes(N, K);
+  s.sfw_stride = nvfp4_scale_bytes(N, sparse ? K / 2 : K);
+  s.meta = meta;
+  s.meta_stride = sparse ? nvfp4_sparse_meta_bytes(N, K) : 0;
   s.sfx = slabs;
   s.ga = ga;
   s.gb = gb;
@@ -675,15 +682,16 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   s.acc_cols = kGroupTileRows;
   s.acc_bufs = 2;
   s.swiglu = swiglu;
-  const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0) - 1536;
+  const int sf_cols = sparse ? 40 : 32;  // TMEM columns per stage: scales (+ metadata)
+  const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0, sparse) - 1536;
   int stages = g_tune.grouped_stages;
   if (stages == 0) stages = (kSmemLimit - 1536 - 256) / stage_bytes;
-  const int tmem_room = (512 - 2 * s.acc_cols) / 32;
+  const int tmem_room = (512 - 2 * s.acc_cols) / sf_cols;
   if (stages > tmem_room) stages = tmem_room;
   if (stages > 16) stages = 16;
-  if (stream_smem_bytes(stages, s.x_rows, 256) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (stream_smem_bytes(stages, s.x_rows, 256, sparse) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   s.stages = stages;
-  s.tmem_cols = pow2_at_least(2 * s.acc_cols + 32 * stages);
+  s.tmem_cols = pow2_at_least(2 * s.acc_cols + sf_cols * stages);
   const int grid = g_tune.grouped_grid ? g_tune.grouped_grid : d.sms;
   rc = from_cuda(launch_stream(tmW, tmX, s, true, grid, st));
   g_last_launches = 2;
@@ -706,6 +714,17 @@ int nvfp4_grouped_gemm_gather(const uint8_t* a_tok, const uint8_t* sfa_tok, cons
   if (!row_token && M_total > 0) return NVFP4_ERR_INVALID_ARG;
   return grouped_impl(a_tok, sfa_tok, ga, b, sfb, gb, expert_offsets, E, M_total, N, K, y, workspace, workspace_bytes,
                       dev_status, stream, 0, row_token, T);
+}
+
+int nvfp4_grouped_sparse_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b_c,
+                              const uint8_t* sfb_c, const uint8_t* meta, const float* gb,
+                              const int32_t* expert_offsets, int32_t E, int64_t M_total, int64_t N, int64_t K,
+                              uint16_t* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              void* stream) {
+  if (!meta && M_total > 0) return NVFP4_ERR_INVALID_ARG;
+  if (meta && !aligned16(meta)) return NVFP4_ERR_ALIGNMENT;
+  return grouped_impl(a, sfa, ga, b_c, sfb_c, gb, expert_offsets, E, M_total, N, K, y, workspace, workspace_bytes,
+                      dev_status, stream, 0, nullptr, 0, meta);
 }
 
 int nvfp4_grouped_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint8_t* b_gu,

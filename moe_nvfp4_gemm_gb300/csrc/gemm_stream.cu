@@ -92,7 +92,7 @@ constexpr uint32_t kStreamHandoffBarrier = 1;
 constexpr uint32_t kStreamEpilogueBarrier = 2;  // the 4 epilogue warps
 
 // VARIANT: bit 0 SwiGLU epilogue, bit 1 token gather in the load stage (grouped only);
-// bit 2 pair-wise 2:4 sparse weights (dense path only): the weight tile holds compressed
+// bit 2 pair-wise 2:4 sparse weights (dense or plain grouped path): the weight tile holds compressed
 // values, a stage spans 512 K elements (four K = 128 sparse MMAs) and carries the metadata
 // tile. Compiled separately so that the plain kernels carry none of them.
 template <bool GROUPED, int VARIANT = 0>
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     r.n16 = (it.rows + 15) >> 4;
     r.sfw = p.sfw + it.e * p.sfw_stride + static_cast<int64_t>(it.wt) * KC4 * 512;
     r.sfx = p.sfx + static_cast<int64_t>(it.slab) * KC4 * 512;
-    r.meta = SPARSE ? p.meta + static_cast<int64_t>(it.wt) * KMC * 4096 : nullptr;
+    r.meta = SPARSE ? p.meta + it.e * p.meta_stride + static_cast<int64_t>(it.wt) * KMC * 4096 : nullptr;
     return r;
   };
   // The token tiles and their scales of stage st_idx = K block kb (sparse: two boxes per row).
@@ -601,7 +601,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
 // Workspace: [0] n_tiles, [16..) int4 tiles[max_tiles], then the slabs (then xg).
 __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict__ offsets,
                                                       const int32_t* __restrict__ row_token, int T, int E, int M_total,
-                                                      int K, const uint8_t* __restrict__ sfx, int32_t* n_tiles_out,
+                                                      int K, int kc4, const uint8_t* __restrict__ sfx,
+                                                      int32_t* n_tiles_out,
                                                       int4* __restrict__ tiles, uint8_t* __restrict__ slabs,
                                                       int32_t* status, const uint8_t* __restrict__ x_tok,
                                                       uint8_t* __restrict__ xg) {
@@ -665,7 +666,7 @@ __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict_
   // tile and row within the tile, and its source row; then the lanes gather the row's
   // scale words (one 4-byte word = four consecutive 16-element blocks) into the tile's
   // slab and, with xg, copy its packed row 16 bytes per lane and step.
-  const int64_t KC4 = K / 64;
+  const int64_t KC4 = kc4;    // 512-byte scale tiles per 128 rows (K / 64; K / 128 for 32-element blocks)
   const int64_t C = K / 32;  // 16-byte chunks per packed row of K / 2 bytes
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
@@ -745,14 +746,16 @@ int stream_smem_bytes(int stages, int x_rows, int recv_bytes, bool sparse) {
 cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, bool grouped, int grid,
                           cudaStream_t st) {
   if (!grouped) return a.meta ? launch_stream_t<false, 4>(tmW, tmX, a, grid, st) : launch_stream_t<false, 0>(tmW, tmX, a, grid, st);
-  if (a.row_token && a.swiglu) return cudaErrorInvalidValue;  // no entry point combines them
+  if ((a.row_token || a.swiglu) && a.meta) return cudaErrorInvalidValue;  // no entry point combines them
+  if (a.row_token && a.swiglu) return cudaErrorInvalidValue;
+  if (a.meta) return launch_stream_t<true, 4>(tmW, tmX, a, grid, st);
   if (a.row_token) return launch_stream_t<true, 2>(tmW, tmX, a, grid, st);
   if (a.swiglu) return launch_stream_t<true, 1>(tmW, tmX, a, grid, st);
   return launch_stream_t<true, 0>(tmW, tmX, a, grid, st);
 }
 
 cudaError_t launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int T, int E, int M_total, int K,
-                                const uint8_t* sfx,
+                                int kc4, const uint8_t* sfx,
                                 int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
                                 cudaStream_t st, const uint8_t* x_tok, uint8_t* xg) {
   const int smem = 2 * (E + 1) * 4;
@@ -760,8 +763,8 @@ cudaError_t launch_grouped_prep(const int32_t* offsets, const int32_t* row_token
     cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_grouped_prep));
     if (e != cudaSuccess) return e;
   }
-  k_grouped_prep<<<grid, 256, smem, st>>>(offsets, row_token, T, E, M_total, K, sfx, n_tiles, tiles, slabs, status,
-                                          x_tok, xg);
+  k_grouped_prep<<<grid, 256, smem, st>>>(offsets, row_token, T, E, M_total, K, kc4, sfx, n_tiles, tiles, slabs,
+                                          status, x_tok, xg);
   return cudaGetLastError();
 }
 

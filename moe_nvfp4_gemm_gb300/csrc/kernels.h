@@ -70,7 +70,8 @@ struct StreamArgs {
   int w_keep;                // weights loaded L2 evict_last (kept resident across calls), else evict_first
   uint64_t watchdog_ns;      // limit of every pipeline wait
   int drop_stage;            // test hook: k >= 1 withholds the k-th stage CTA 0 loads (0: none)
-  const uint8_t* meta;       // dense path, pair-wise 2:4 sparse weights: tiled metadata (null: dense)
+  const uint8_t* meta;       // pair-wise 2:4 sparse weights: tiled metadata (null: dense weights)
+  int64_t meta_stride;       // grouped: bytes of metadata per expert
 };
 
 
@@ -93,7 +94,7 @@ cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, co
 cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, bool grouped,
                           int grid, cudaStream_t st);
 cudaError_t launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int T, int E, int M_total, int K,
-                                const uint8_t* sfx,
+                                int kc4, const uint8_t* sfx,
                                 int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
                                 cudaStream_t st, const uint8_t* x_tok = nullptr, uint8_t* xg = nullptr);
 int stream_smem_bytes(int stages, int x_rows, int recv_bytes, bool sparse = false);

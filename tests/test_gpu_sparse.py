@@ -136,3 +136,73 @@ def test_sparse_decode_full_size_sampled(M):
     rng = np.random.default_rng(M)
     cols = np.concatenate([[0, 127, 128, 8191], rng.choice(8192, 252, replace=False)])
     g.check(y, cols=cols)
+
+
+class GroupedSparse:
+    def __init__(self, counts, N, K, seed, a_rows=None, w=None):
+        E = len(counts)
+        self.E, self.N, self.K = E, N, K
+        self.off = np.zeros(E + 1, dtype=np.int32)
+        self.off[1:] = np.cumsum(counts)
+        self.Mt = int(self.off[-1])
+        if a_rows is None:
+            a_rows = synth.normal_bf16((max(self.Mt, 1), K), 2 * seed, 1.0)[: self.Mt]
+        if w is None:
+            w = lambda e: synth.moe_expert_weight(e, N, K, seed)
+        self.xq, self.xsf, self.gx = oracle.quantize_b32(a_rows)
+        ws = [oracle.sparse_quantize_weight(w(e)) for e in range(E)]
+        self.cq = np.stack([t[0] for t in ws])
+        self.csf = np.stack([t[1] for t in ws])
+        self.gw = np.array([t[2] for t in ws], np.float32)
+        self.meta = np.stack([t[3] for t in ws])
+        self.meta_t = np.stack([oracle.meta_tile(self.meta[e], N, K) for e in range(E)])
+
+    def run(self, status=None, offsets=None):
+        off = self.off if offsets is None else offsets
+        y = m.nvfp4_grouped_sparse_gemm(to_dev(self.xq), to_dev(self.xsf), scalar(self.gx), to_dev(self.cq),
+                                        to_dev(self.csf), to_dev(self.meta_t), to_dev(self.gw), to_dev(off), self.E,
+                                        self.Mt, self.N, self.K, dev_status=status)
+        torch.cuda.synchronize()
+        return y
+
+    def check(self, y, rows=None, cols=None):
+        yr, ad = oracle.grouped_sparse_gemm(self.xq, self.xsf, self.gx, self.cq, self.csf, self.meta, self.gw,
+                                            self.off, self.E, self.Mt, self.N, self.K, rows=rows, cols=cols)
+        yg = y.float().cpu().numpy()
+        if rows is not None:
+            yg = yg[np.asarray(rows)]
+        if cols is not None:
+            yg = yg[:, np.asarray(cols)]
+        ok, worst = oracle.within_tolerance(yg, yr, ad)
+        assert ok, f"grouped sparse parity failed: worst ratio {worst}"
+
+
+@pytest.mark.parametrize("counts,N,K", [
+    ((3, 0, 17, 1, 0, 9), 256, 512),
+    ((64, 65, 63, 1, 127, 128, 129, 0), 136, 1024),
+    ((0, 300, 0), 128, 640),
+    ((5,), 8, 128),
+])
+def test_grouped_sparse_matches_oracle(counts, N, K):
+    g = GroupedSparse(counts, N, K, 91)
+    g.check(g.run())
+
+
+def test_grouped_sparse_bad_offsets_reported():
+    g = GroupedSparse((4, 4), 128, 512, 92)
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    g.run(status=st, offsets=np.array([0, 5, 4], dtype=np.int32))
+    assert st.item() == -8
+
+
+def test_grouped_sparse_moe_workload_sampled():
+    # the MoE workload with pair-wise 2:4 sparse experts: 256 experts, 512 tokens top-8
+    # (4096 routed rows), K = 6144, N = 4096
+    a_rows, off, _ = synth.moe_tokens(512, 256, 8, 6144, 3)
+    g = GroupedSparse(tuple(np.diff(off)), 4096, 6144, 3, a_rows=a_rows,
+                      w=lambda e: synth.moe_expert_weight(e, 4096, 6144, 3))
+    y = g.run()
+    rng = np.random.default_rng(13)
+    rows = np.concatenate([[0, g.Mt - 1], rng.choice(g.Mt, 22, replace=False)])
+    cols = np.concatenate([[0, 127, 128, 4095], rng.choice(4096, 36, replace=False)])
+    g.check(y, rows=rows, cols=cols)
