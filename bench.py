@@ -680,6 +680,7 @@ def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
                                                    y=y, workspace=wsp), 4, 5, stream)
     hit = int((np.diff(off) > 0).sum())
     mbytes = hit * (N * K // 2 + sfb_bytes)
+    mbytes_uniform = mbytes
     gbs = mbytes / (ms * 1e-3) / 1e9
     out["moe_grouped"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
                           "hbm_frac_vs_8TBps": gbs / NOMINAL_HBM_GBS,
@@ -758,6 +759,37 @@ def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
                        "layer_weight_GBps": (mbytes + dbytes) / (ms_layer * 1e-3) / 1e9,
                        "layer_hbm_frac": (mbytes + dbytes) / (ms_layer * 1e-3) / 1e9 / hbm}
     del y_act, qd, sd, y_dn
+    # pair-wise 2:4 sparse experts: each expert's weight pruned, compressed and quantised on the
+    # GPU; the routed rows quantised in 32-element blocks
+    cqs = torch.empty((E, N, K // 4), dtype=torch.uint8, device=dev)
+    csb = m.nvfp4_scale_bytes(N, K // 2)
+    csfs = torch.empty((E, csb), dtype=torch.uint8, device=dev)
+    gws = torch.empty(E, dtype=torch.float32, device=dev)
+    mb = m.nvfp4_sparse_meta_bytes(N, K)
+    metas = torch.empty((E, mb), dtype=torch.uint8, device=dev)
+    for e in range(E):
+        c, meta = m.nvfp4_prune_pairs(to_dev(synth.moe_expert_weight(e, N, K, 3)))
+        _, g_c = m.nvfp4_amax(c)
+        cq, csf = m.nvfp4_quantize(c, g_c)
+        cqs[e].copy_(cq)
+        csfs[e].copy_(csf)
+        gws[e:e + 1].copy_(g_c)
+        metas[e].copy_(meta)
+    a_d = to_dev(a_rows)
+    _, gxs = m.nvfp4_amax(a_d)
+    xq32, xsf32 = m.nvfp4_quantize_b32(a_d, gxs)
+    del a_d
+    ms = time_graph(lambda i: m.nvfp4_grouped_sparse_gemm(xq32, xsf32, gxs, cqs, csfs, metas, gws, off_d, E, Mt, N,
+                                                          K, y=y, workspace=wsp), 4, 5, stream)
+    sbytes = hit * (N * K // 4 + csb + mb)
+    gbs = sbytes / (ms * 1e-3) / 1e9
+    out["moe_grouped_sparse"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
+                                 "bytes": sbytes, "bytes_dense": mbytes_uniform,
+                                 "speedup_vs_dense": out["moe_grouped"]["us"] / (ms * 1e3),
+                                 "tflops_dense_equivalent": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12,
+                                 "format": "pair-wise 2:4 experts (values [N, K/2] NVFP4 + 4-bit metadata per 8 K); "
+                                           "routed rows in 32-element blocks"}
+    del cqs, csfs, metas, xq32, xsf32
     a_s, off_s, _ = synth.moe_tokens(512, E, 8, K, 3, zipf_s=1.0)
     qs, sfs, gs = quantize_dev(to_dev(a_s))
     off_sd = to_dev(off_s)
