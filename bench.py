@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--no-breakdown", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--sustained-seconds", type=float, default=3.0)
-    ap.add_argument("--only", choices=["square", "decode", "moe", "prefill", "tiny"], default=None,
+    ap.add_argument("--only", choices=["square", "decode", "moe", "prefill", "tiny", "sparse"], default=None,
                     help="run only this breakdown workload (for profiling) and print its numbers")
     return ap.parse_args()
 
@@ -565,8 +565,12 @@ def run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak, 
     hbm = peaks["hbm"]
     if only in (None, "decode"):
         run_decode(m, synth, dev, stream, to_dev, quantize_dev, hbm, out)
+    if only in (None, "decode", "sparse"):
+        run_decode_sparse(m, synth, dev, stream, to_dev, hbm, out)
     if only in (None, "moe"):
         run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out)
+    if only in (None, "moe", "sparse"):
+        run_moe_sparse(m, synth, dev, stream, to_dev, hbm, out)
     if only in (None, "prefill"):
         run_prefill(m, synth, dev, stream, to_dev, quantize_dev, hbm, fp4_peak, out)
     if only in (None, "tiny"):
@@ -579,6 +583,7 @@ def run_decode(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
     # decode: M in {1, 16, 32}, N = K = 8192; 8 rotating weight copies (302 MB > L2)
     w_bits = synth.normal_bf16((SQ, SQ), 2 * 2 + 1, 0.02)
     wq, sfw, gw = quantize_dev(to_dev(w_bits))
+    del w_bits
     copies = [(wq.clone(), sfw.clone()) for _ in range(8)]
     wbytes = wq.numel() + sfw.numel()
     for M in (1, 16, 32):
@@ -626,9 +631,14 @@ def run_decode(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
                           "hot-call time = step time - cold-only step time",
                 "note": "kept: hot weight loaded L2 evict_last (NVFP4_TUNE_WEIGHT_L2=1), cold ones evict_first"}
     del copies, wq, sfw
-    # pair-wise 2:4 sparse weights on the sparse tensor cores: the same weight pruned, compressed
-    # and quantised on the GPU (values [N, K/2] as NVFP4, tiled metadata), activations in
-    # 32-element blocks; 8 rotating copies, CUDA graph of 16 calls
+
+
+def run_decode_sparse(m, synth, dev, stream, to_dev, hbm, out):
+    """Decode M = 1/16/32, N = K = 8192 with pair-wise 2:4 sparse weights: the decode
+    workload's weight pruned, compressed and quantised on the GPU (values [N, K/2] as NVFP4,
+    tiled metadata), activations in 32-element blocks; 8 rotating copies, graph of 16 calls."""
+    import torch
+    w_bits = synth.normal_bf16((SQ, SQ), 2 * 2 + 1, 0.02)
     wd = to_dev(w_bits)
     c, meta = m.nvfp4_prune_pairs(wd)
     _, g_c = m.nvfp4_amax(c)
@@ -645,14 +655,16 @@ def run_decode(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
                                            M, SQ, SQ, y=y)
         ms = time_graph(fn, 16, 20, stream)
         gbs = sbytes / (ms * 1e-3) / 1e9
-        dense_us = out[f"decode_M{M}"]["us"]
+        dense = out.get(f"decode_M{M}")
         out[f"decode_sparse_M{M}"] = {
             "us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "bytes": sbytes,
-            "bytes_dense": out[f"decode_M{M}"]["bytes"], "speedup_vs_dense": dense_us / (ms * 1e3),
+            "bytes_dense": 37748736, "speedup_vs_dense": dense["us"] / (ms * 1e3) if dense else None,
             "format": "pair-wise 2:4 (2 of 4 pairs per 8 K): values [N, K/2] NVFP4 + 4-bit metadata per 8 K; "
                       "activations in 32-element blocks",
             "timing": "CUDA graph of 16 calls over 8 weight copies"}
     del scopies, cq, csf, meta
+
+
 
 
 def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
@@ -680,7 +692,6 @@ def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
                                                    y=y, workspace=wsp), 4, 5, stream)
     hit = int((np.diff(off) > 0).sum())
     mbytes = hit * (N * K // 2 + sfb_bytes)
-    mbytes_uniform = mbytes
     gbs = mbytes / (ms * 1e-3) / 1e9
     out["moe_grouped"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
                           "hbm_frac_vs_8TBps": gbs / NOMINAL_HBM_GBS,
@@ -759,8 +770,33 @@ def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
                        "layer_weight_GBps": (mbytes + dbytes) / (ms_layer * 1e-3) / 1e9,
                        "layer_hbm_frac": (mbytes + dbytes) / (ms_layer * 1e-3) / 1e9 / hbm}
     del y_act, qd, sd, y_dn
-    # pair-wise 2:4 sparse experts: each expert's weight pruned, compressed and quantised on the
-    # GPU; the routed rows quantised in 32-element blocks
+    a_s, off_s, _ = synth.moe_tokens(512, E, 8, K, 3, zipf_s=1.0)
+    qs, sfs, gs = quantize_dev(to_dev(a_s))
+    off_sd = to_dev(off_s)
+    ms = time_graph(lambda i: m.nvfp4_grouped_gemm(qs, sfs, gs, qb, sfb, gb, off_sd, E, Mt, N, K,
+                                                   y=y, workspace=wsp), 4, 5, stream)
+    hit = int((np.diff(off_s) > 0).sum())
+    mbytes = hit * (N * K // 2 + sfb_bytes)
+    gbs = mbytes / (ms * 1e-3) / 1e9
+    out["moe_grouped_skewed"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
+                                 "hbm_frac_vs_8TBps": gbs / NOMINAL_HBM_GBS,
+                                 "max_rows_per_expert": int(np.diff(off_s).max()), "routing": "Zipf(1) popularity",
+                                 "bytes": mbytes, "tflops": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12}
+    del qb, sfb, wsp
+    torch.cuda.empty_cache()
+
+
+def run_moe_sparse(m, synth, dev, stream, to_dev, hbm, out):
+    """The MoE workload with pair-wise 2:4 sparse experts: each expert's weight pruned,
+    compressed and quantised on the GPU, the routed rows quantised in 32-element blocks."""
+    import torch
+    E, N, K = 256, 4096, 6144
+    a_rows, off, _ = synth.moe_tokens(512, E, 8, K, 3)
+    Mt = int(off[-1])
+    off_d = to_dev(off)
+    hit = int((np.diff(off) > 0).sum())
+    y = torch.empty((Mt, N), dtype=torch.bfloat16, device=dev)
+    wsp = torch.empty(m.nvfp4_grouped_gemm_workspace_bytes(E, Mt, N, K), dtype=torch.uint8, device=dev)
     cqs = torch.empty((E, N, K // 4), dtype=torch.uint8, device=dev)
     csb = m.nvfp4_scale_bytes(N, K // 2)
     csfs = torch.empty((E, csb), dtype=torch.uint8, device=dev)
@@ -784,25 +820,14 @@ def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
     sbytes = hit * (N * K // 4 + csb + mb)
     gbs = sbytes / (ms * 1e-3) / 1e9
     out["moe_grouped_sparse"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
-                                 "bytes": sbytes, "bytes_dense": mbytes_uniform,
-                                 "speedup_vs_dense": out["moe_grouped"]["us"] / (ms * 1e3),
+                                 "bytes": sbytes, "bytes_dense": hit * (N * K // 2 + m.nvfp4_scale_bytes(N, K)),
+                                 "speedup_vs_dense": (out["moe_grouped"]["us"] / (ms * 1e3)
+                                                      if "moe_grouped" in out else None),
                                  "tflops_dense_equivalent": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12,
                                  "format": "pair-wise 2:4 experts (values [N, K/2] NVFP4 + 4-bit metadata per 8 K); "
                                            "routed rows in 32-element blocks"}
     del cqs, csfs, metas, xq32, xsf32
-    a_s, off_s, _ = synth.moe_tokens(512, E, 8, K, 3, zipf_s=1.0)
-    qs, sfs, gs = quantize_dev(to_dev(a_s))
-    off_sd = to_dev(off_s)
-    ms = time_graph(lambda i: m.nvfp4_grouped_gemm(qs, sfs, gs, qb, sfb, gb, off_sd, E, Mt, N, K,
-                                                   y=y, workspace=wsp), 4, 5, stream)
-    hit = int((np.diff(off_s) > 0).sum())
-    mbytes = hit * (N * K // 2 + sfb_bytes)
-    gbs = mbytes / (ms * 1e-3) / 1e9
-    out["moe_grouped_skewed"] = {"us": ms * 1e3, "weight_GBps": gbs, "hbm_frac": gbs / hbm, "experts_hit": hit,
-                                 "hbm_frac_vs_8TBps": gbs / NOMINAL_HBM_GBS,
-                                 "max_rows_per_expert": int(np.diff(off_s).max()), "routing": "Zipf(1) popularity",
-                                 "bytes": mbytes, "tflops": 2.0 * Mt * N * K / (ms * 1e-3) / 1e12}
-    del qb, sfb, wsp
+    del y, wsp
     torch.cuda.empty_cache()
 
 
