@@ -348,6 +348,14 @@ int nvfp4_encode_e4m3(const float* v, int64_t n, uint8_t* out, void* stream);
  *                              wait gives up, stops the CTA's other roles, frees its tensor
  *                              memory and reports NVFP4_ERR_TIMEOUT in *dev_status (0: the
  *                              default, 2 s). Applies to the launches that follow.
+ *   NVFP4_TUNE_STREAM_L2_PREFETCH  decode-M kernels: K blocks (of 256 K elements, 512 when
+ *                              sparse) of each CTA's weight slice prefetched into L2 when the
+ *                              CTA starts, ahead of the launch-dependency wait. 0 (default): the
+ *                              whole slice; -1: none. A prefetch moves no data into the kernel,
+ *                              so results and stream order are unchanged.
+ *   NVFP4_TUNE_GROUPED_TILE_ROWS  token rows of one expert per grouped work item: 128 (the
+ *                              default) or 64. An expert with r routed rows streams its weights
+ *                              ceil(r / tile rows) times. Results are unchanged.
  *   NVFP4_TUNE_TEST_WITHHOLD_STAGE  test hook for the timeout path: k >= 1 makes the first CTA
  *                              of each GEMM kernel withhold the loads of the k-th pipeline stage
  *                              it would request, so that stage never arrives and the waits run
@@ -367,7 +375,9 @@ enum {
   NVFP4_TUNE_WEIGHT_L2 = 10,
   NVFP4_TUNE_DENSE_RASTER = 11,
   NVFP4_TUNE_WATCHDOG_US = 12,
-  NVFP4_TUNE_TEST_WITHHOLD_STAGE = 13
+  NVFP4_TUNE_TEST_WITHHOLD_STAGE = 13,
+  NVFP4_TUNE_STREAM_L2_PREFETCH = 14,
+  NVFP4_TUNE_GROUPED_TILE_ROWS = 15
 };
 int nvfp4_tune(int key, int value);
 

@@ -30,6 +30,8 @@ NVFP4_TUNE_WEIGHT_L2 = 10
 NVFP4_TUNE_DENSE_RASTER = 11
 NVFP4_TUNE_WATCHDOG_US = 12
 NVFP4_TUNE_TEST_WITHHOLD_STAGE = 13
+NVFP4_TUNE_STREAM_L2_PREFETCH = 14
+NVFP4_TUNE_GROUPED_TILE_ROWS = 15
 
 STATUS = {0: "NVFP4_OK", -1: "NVFP4_ERR_INVALID_ARG", -2: "NVFP4_ERR_UNSUPPORTED_SHAPE",
           -3: "NVFP4_ERR_ALIGNMENT", -4: "NVFP4_ERR_ARCH", -5: "NVFP4_ERR_CUDA",

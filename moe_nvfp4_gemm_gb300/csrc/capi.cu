@@ -44,7 +44,8 @@ thread_local int g_last_launches = 0;
 
 struct Tune {
   int dense_bn = 0, dense_grid = 0, stream_max_m = 0, stream_split = 0, stream_stages = 0, grouped_grid = 0,
-      grouped_stages = 0, dense_kernel = 0, pdl = 0, weight_l2 = 0, dense_raster = 0, watchdog_us = 0, withhold_stage = 0;
+      grouped_stages = 0, dense_kernel = 0, pdl = 0, weight_l2 = 0, dense_raster = 0, watchdog_us = 0, withhold_stage = 0,
+      stream_l2_prefetch = 0, grouped_tile_rows = 0;
 } g_tune;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -140,6 +141,8 @@ int stream_pdl_mode() { return g_tune.pdl == 0 ? 2 : (g_tune.pdl < 0 ? 0 : g_tun
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
 
+// K blocks of each decode CTA's weight slice prefetched into L2 at entry (all of them by default).
+int stream_l2_prefetch() { return g_tune.stream_l2_prefetch == 0 ? (1 << 20) : (g_tune.stream_l2_prefetch < 0 ? 0 : g_tune.stream_l2_prefetch); }
 uint64_t watchdog_ns() { return g_tune.watchdog_us ? uint64_t(g_tune.watchdog_us) * 1000u : kWatchdogNs; }
 
 int64_t pad16(int64_t v) { return (v + 15) / 16 * 16; }
@@ -227,6 +230,14 @@ int nvfp4_tune(int key, int value) {
     case NVFP4_TUNE_TEST_WITHHOLD_STAGE:
       if (value < 0) return NVFP4_ERR_INVALID_ARG;
       g_tune.withhold_stage = value;
+      return NVFP4_OK;
+    case NVFP4_TUNE_STREAM_L2_PREFETCH:
+      if (value < -1) return NVFP4_ERR_INVALID_ARG;
+      g_tune.stream_l2_prefetch = value;
+      return NVFP4_OK;
+    case NVFP4_TUNE_GROUPED_TILE_ROWS:
+      if (value != 0 && value != 64 && value != 128) return NVFP4_ERR_INVALID_ARG;
+      g_tune.grouped_tile_rows = value;
       return NVFP4_OK;
     case NVFP4_TUNE_DENSE_RASTER:
       if (value < -1 || value > 1024) return NVFP4_ERR_INVALID_ARG;
@@ -355,6 +366,7 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
     s.w_keep = g_tune.weight_l2;
     s.watchdog_ns = watchdog_ns();
     s.drop_stage = g_tune.withhold_stage;
+    s.l2_prefetch = stream_l2_prefetch();
     const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0) - 1536;
     const int recv_bytes = stream_recv_bytes(s.M, split);
     int stages = g_tune.stream_stages;
@@ -550,6 +562,7 @@ int nvfp4_sparse_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, con
     s.w_keep = g_tune.weight_l2;
     s.watchdog_ns = watchdog_ns();
     s.drop_stage = g_tune.withhold_stage;
+    s.l2_prefetch = stream_l2_prefetch();
     const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0, true) - 1536;
     const int recv_bytes = stream_recv_bytes(s.M, split);
     int stages = g_tune.stream_stages;
@@ -636,12 +649,16 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   uint8_t* xg = nullptr;
   if (row_token && workspace_bytes >= nvfp4_grouped_gemm_gather_workspace_bytes(E, M_total, N, K))
     xg = ws + gathered_rows_offset(E, M_total, N, K);
+  // token rows per work item: up to 128, so that a heavily routed expert streams its
+  // weights ceil(rows / 128) times
+  const int tile_rows = g_tune.grouped_tile_rows ? g_tune.grouped_tile_rows : kGroupTileMax;
   // one warp per routed row and step (eight per block)
   const int64_t prep_blocks = (M_total + 7) / 8;
   int prep_grid = static_cast<int>(prep_blocks < 4 * d.sms ? prep_blocks : 4 * d.sms);
   if (prep_grid < 1) prep_grid = 1;
   rc = from_cuda(launch_grouped_prep(expert_offsets, row_token, static_cast<int>(T), E, static_cast<int>(M_total),
-                                     static_cast<int>(K), static_cast<int>(sparse ? K / 128 : K / 64), sfa, n_tiles,
+                                     static_cast<int>(K), static_cast<int>(sparse ? K / 128 : K / 64), tile_rows, sfa,
+                                     n_tiles,
                                      tiles, slabs, dev_status, prep_grid, st, xg ? a : nullptr, xg));
   g_last_launches = 1;
   if (rc) return rc;
@@ -678,18 +695,19 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   s.w_keep = g_tune.weight_l2;
   s.watchdog_ns = watchdog_ns();
   s.drop_stage = g_tune.withhold_stage;
-  s.x_rows = kGroupTileRows;
-  s.acc_cols = kGroupTileRows;
+  s.x_rows = tile_rows;
+  s.acc_cols = tile_rows;
   s.acc_bufs = 2;
   s.swiglu = swiglu;
   const int sf_cols = sparse ? 40 : 32;  // TMEM columns per stage: scales (+ metadata)
   const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0, sparse) - 1536;
   int stages = g_tune.grouped_stages;
-  if (stages == 0) stages = (kSmemLimit - 1536 - 256) / stage_bytes;
+  if (stages == 0) stages = (kSmemLimit - 1536 - grouped_extra_bytes(tile_rows)) / stage_bytes;
   const int tmem_room = (512 - 2 * s.acc_cols) / sf_cols;
   if (stages > tmem_room) stages = tmem_room;
   if (stages > 16) stages = 16;
-  if (stream_smem_bytes(stages, s.x_rows, 256, sparse) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (stream_smem_bytes(stages, s.x_rows, grouped_extra_bytes(tile_rows), sparse) > kSmemLimit)
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
   s.stages = stages;
   s.tmem_cols = pow2_at_least(2 * s.acc_cols + sf_cols * stages);
   const int grid = g_tune.grouped_grid ? g_tune.grouped_grid : d.sms;

@@ -243,6 +243,18 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     // Weights kept in L2: the first ring carries the evict_last hint as well (its policy
     // costs this thread ~0.6 us), so that none of the matrix is left at normal priority.
     const uint64_t keep = p.w_keep ? policy_evict_last() : 0;
+    // The CTA's weight slice is prefetched into L2 first: under a programmatic dependency
+    // those reads overlap the tail of the previous kernel, and the ring's loads then find
+    // the bytes in L2 (the first ring itself when the weights are requested directly).
+    {
+      const int npf = GROUPED ? 0 : min(p.l2_prefetch, first_it.kb1 - first_it.kb0);
+      for (int j = p.pdl == 1 ? n_pre : 0; j < npf; ++j) {
+        const int kb = first_it.kb0 + j;
+        tma_prefetch_2d(&tmW, kb * 128, src.wrow0);
+        bulk_prefetch_l2(src.sfw + kb * 2048, min(4, (K - kb * KSTAGE) / KMMA) * 512);
+        if (SPARSE) bulk_prefetch_l2(src.meta + kb * 4096, 4096);
+      }
+    }
     if (p.pdl == 2) griddep_wait();  // set-up-only overlap: no load before the previous kernel completes
     for (int j = 0; j < n_pre; ++j)
       if (!(blockIdx.x == 0 && j + 1 == p.drop_stage))  // test hook: stage withheld
@@ -296,22 +308,26 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     int pend_stage[16], pend_kb[16], npend = 0;
     Item it;
     auto load_tokens = [&](const Item& x) {
-      return make_int2(__ldg(p.row_token + x.row0 + min(lane, x.rows - 1)),
-                       __ldg(p.row_token + x.row0 + min(lane + 32, x.rows - 1)));
+      return make_int4(__ldg(p.row_token + x.row0 + min(lane, x.rows - 1)),
+                       __ldg(p.row_token + x.row0 + min(lane + 32, x.rows - 1)),
+                       __ldg(p.row_token + x.row0 + min(lane + 64, x.rows - 1)),
+                       __ldg(p.row_token + x.row0 + min(lane + 96, x.rows - 1)));
     };
-    int2 tok_regs = make_int2(0, 0);
+    int4 tok_regs = make_int4(0, 0, 0, 0);
     bool tok_ready = false;
     for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it) && !*abort_flag; i += stride) {
       const Src src = item_src(it);
       const int n16 = src.n16;
       const uint8_t* sfx = src.sfx;
       if (GROUPED && (VARIANT & 2)) {
-        // this item's token rows (loaded during the previous item, two per lane); rows past
+        // this item's token rows (loaded during the previous item, four per lane); rows past
         // the tile's count repeat its last row (their accumulator columns are never stored),
         // indices clamped into x (prep reports bad ones)
         if (!tok_ready) tok_regs = load_tokens(it);
         tok_idx[lane] = min(max(tok_regs.x, 0), p.T - 1);
         tok_idx[lane + 32] = min(max(tok_regs.y, 0), p.T - 1);
+        tok_idx[lane + 64] = min(max(tok_regs.z, 0), p.T - 1);
+        tok_idx[lane + 96] = min(max(tok_regs.w, 0), p.T - 1);
         __syncwarp();
         Item nx;  // start the next item's index loads now; they land while this item streams
         tok_ready = get_item<GROUPED>(p, i + stride, n_items, NT, KB, nx);
@@ -442,7 +458,6 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     volatile int32_t dummy = 0;
     mbar_wait_warp(drain, 0, &dummy, wd);
   } else {
-    constexpr int MAXC = kGroupTile;
     if (warp == 2) {
       // Weights are read once per call: evict_first keeps them from displacing the token
       // tiles (evict_last) and other data, unless the caller asks to keep them in L2.
@@ -472,39 +487,39 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
       const bool has_k = it.kb1 > it.kb0;
       const uint32_t tbase = tmem + buf * p.acc_cols + (static_cast<uint32_t>(q * 32) << 16);
       if (GROUPED) {
-        // all of this item's columns into registers, release the accumulator for the
-        // next item's MMAs, then store
-        uint32_t r[MAXC];
+        // 32 columns (token rows) at a time: drained, scaled and stored; the accumulator
+        // is released after the last chunk while the other buffer keeps the MMAs busy
+        for (int c = 0; c < n_mma; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(tbase + c, r);
+          tmem_ld_wait();
+          if (VARIANT & 1) {
+            // Weight rows 2c and 2c + 1 (gate and up of output column c) sit in adjacent
+            // lanes: the even lane takes its partner's value and writes silu(gate) * up.
+            const int n_out = N >> 1;
 #pragma unroll
-        for (int c = 0; c < MAXC; c += 32)
-          if (c < n_mma) tmem_ld32(tbase + c, r + c);
-        tmem_ld_wait();
+            for (int j = 0; j < 32; ++j)
+              if (c + j < it.rows) {
+                const float v = __uint_as_float(r[j]) * alpha;
+                const float up = __shfl_xor_sync(0xffffffffu, v, 1);
+                if ((lane & 1) == 0 && wrow < N) {
+                  const float act = v / (1.0f + __expf(-v));
+                  p.y[static_cast<int64_t>(it.row0 + c + j) * n_out + (wrow >> 1)] =
+                      __bfloat16_as_ushort(__float2bfloat16_rn(act * up));
+                }
+              }
+          } else if (wrow < N) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (c + j < it.rows)
+                p.y[static_cast<int64_t>(it.row0 + c + j) * N + wrow] =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j]) * alpha));
+          }
+        }
         tc_fence_before();
         __syncwarp();
         if (elect_one()) mbar_arrive(&tempty[buf]);
         __syncwarp();
-        if (VARIANT & 1) {
-          // Weight rows 2c and 2c + 1 (gate and up of output column c) sit in adjacent
-          // lanes: the even lane takes its partner's value and writes silu(gate) * up.
-          const int n_out = N >> 1;
-#pragma unroll
-          for (int j = 0; j < MAXC; ++j)
-            if (j < it.rows) {
-              const float v = __uint_as_float(r[j]) * alpha;
-              const float up = __shfl_xor_sync(0xffffffffu, v, 1);
-              if ((lane & 1) == 0 && wrow < N) {
-                const float act = v / (1.0f + __expf(-v));
-                p.y[static_cast<int64_t>(it.row0 + j) * n_out + (wrow >> 1)] =
-                    __bfloat16_as_ushort(__float2bfloat16_rn(act * up));
-              }
-            }
-        } else if (wrow < N) {
-#pragma unroll
-          for (int j = 0; j < MAXC; ++j)
-            if (j < it.rows)
-              p.y[static_cast<int64_t>(it.row0 + j) * N + wrow] =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j]) * alpha));
-        }
       } else {
         // one item per CTA: drain 32 columns at a time (fewer live registers)
         for (int c = 0; c < n_mma; c += 32) {
@@ -593,7 +608,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
 
 // ---- grouped preparation ------------------------------------------------------------
 
-// Validates expert_offsets, lists the token tiles (<= kGroupTile rows of one
+// Validates expert_offsets, lists the token tiles (<= tile_rows rows of one
 // expert each; experts without rows get none) and gathers each tile's token
 // scales into its own slab in the 128-row tiled layout, rows starting at 0.
 // With xg: also copies packed token row row_token[r] of x_tok to row r of xg
@@ -601,8 +616,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
 // Workspace: [0] n_tiles, [16..) int4 tiles[max_tiles], then the slabs (then xg).
 __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict__ offsets,
                                                       const int32_t* __restrict__ row_token, int T, int E, int M_total,
-                                                      int K, int kc4, const uint8_t* __restrict__ sfx,
-                                                      int32_t* n_tiles_out,
+                                                      int K, int kc4, int tile_rows,
+                                                      const uint8_t* __restrict__ sfx, int32_t* n_tiles_out,
                                                       int4* __restrict__ tiles, uint8_t* __restrict__ slabs,
                                                       int32_t* status, const uint8_t* __restrict__ x_tok,
                                                       uint8_t* __restrict__ xg) {
@@ -634,7 +649,7 @@ __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict_
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int e0 = min(E, static_cast<int>(threadIdx.x) * per), e1 = min(E, e0 + per);
     int mine = 0;
-    for (int e = e0; e < e1; ++e) mine += (off[e + 1] - off[e] + kGroupTile - 1) / kGroupTile;
+    for (int e = e0; e < e1; ++e) mine += (off[e + 1] - off[e] + tile_rows - 1) / tile_rows;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     int incl = mine;  // inclusive scan within the warp
 #pragma unroll
@@ -649,7 +664,7 @@ __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict_
     int acc = before + incl - mine;
     for (int e = e0; e < e1; ++e) {
       tbase[e] = acc;
-      acc += (off[e + 1] - off[e] + kGroupTile - 1) / kGroupTile;
+      acc += (off[e + 1] - off[e] + tile_rows - 1) / tile_rows;
     }
     if (threadIdx.x == blockDim.x - 1) tbase[E] = before + incl;
   }
@@ -657,8 +672,8 @@ __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict_
   if (blockIdx.x == 0) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
       const int cnt = off[e + 1] - off[e];
-      for (int t = 0; t * kGroupTile < cnt; ++t)
-        tiles[tbase[e] + t] = make_int4(e, off[e] + t * kGroupTile, min(kGroupTile, cnt - t * kGroupTile), tbase[e] + t);
+      for (int t = 0; t * tile_rows < cnt; ++t)
+        tiles[tbase[e] + t] = make_int4(e, off[e] + t * tile_rows, min(tile_rows, cnt - t * tile_rows), tbase[e] + t);
     }
     if (threadIdx.x == 0) *n_tiles_out = tbase[E];
   }
@@ -678,8 +693,8 @@ __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict_
     }
     while (off[lo + 1] <= m) ++lo;  // skip empty experts sharing the same offset
     const int j = m - off[lo];
-    const int64_t tile = tbase[lo] + j / kGroupTile;
-    const int r = j % kGroupTile;
+    const int64_t tile = tbase[lo] + j / tile_rows;
+    const int r = j % tile_rows;
     int src = m;  // the row of x (and of its scales) this routed row reads
     if (row_token) {
       src = __ldg(row_token + m);
@@ -705,8 +720,8 @@ __global__ void __launch_bounds__(256) k_grouped_prep(const int32_t* __restrict_
 template <bool GROUPED, int VARIANT>
 static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, int grid,
                                    cudaStream_t st) {
-  // grouped: 256 bytes of token indices (the token gather); dense: the reduction's receive area
-  const int smem = stream_smem_bytes(a.stages, a.x_rows, GROUPED ? 256 : stream_recv_bytes(a.M, a.split),
+  // grouped: the token indices of a tile (the token gather); dense: the reduction's receive area
+  const int smem = stream_smem_bytes(a.stages, a.x_rows, GROUPED ? grouped_extra_bytes(a.x_rows) : stream_recv_bytes(a.M, a.split),
                                      (VARIANT & 4) != 0);
   cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_gemm_stream<GROUPED, VARIANT>));
   if (e != cudaSuccess) return e;
@@ -739,6 +754,8 @@ static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tm
 // Receive area of the one-way split-K reduction: S slots of ceil(M / S) tokens x 128 fp32.
 int stream_recv_bytes(int M, int split) { return split > 1 ? split * ((M + split - 1) / split) * 512 : 0; }
 
+int grouped_extra_bytes(int x_rows) { return x_rows * 4 > 256 ? x_rows * 4 : 256; }
+
 int stream_smem_bytes(int stages, int x_rows, int recv_bytes, bool sparse) {
   return stages * StreamLayout(x_rows, sparse).stage_bytes + recv_bytes + 1024 + 512;
 }
@@ -755,7 +772,7 @@ cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const 
 }
 
 cudaError_t launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int T, int E, int M_total, int K,
-                                int kc4, const uint8_t* sfx,
+                                int kc4, int tile_rows, const uint8_t* sfx,
                                 int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
                                 cudaStream_t st, const uint8_t* x_tok, uint8_t* xg) {
   const int smem = 2 * (E + 1) * 4;
@@ -763,8 +780,8 @@ cudaError_t launch_grouped_prep(const int32_t* offsets, const int32_t* row_token
     cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_grouped_prep));
     if (e != cudaSuccess) return e;
   }
-  k_grouped_prep<<<grid, 256, smem, st>>>(offsets, row_token, T, E, M_total, K, kc4, sfx, n_tiles, tiles, slabs,
-                                          status, x_tok, xg);
+  k_grouped_prep<<<grid, 256, smem, st>>>(offsets, row_token, T, E, M_total, K, kc4, tile_rows, sfx, n_tiles,
+                                          tiles, slabs, status, x_tok, xg);
   return cudaGetLastError();
 }
 

@@ -72,10 +72,14 @@ struct StreamArgs {
   int drop_stage;            // test hook: k >= 1 withholds the k-th stage CTA 0 loads (0: none)
   const uint8_t* meta;       // pair-wise 2:4 sparse weights: tiled metadata (null: dense weights)
   int64_t meta_stride;       // grouped: bytes of metadata per expert
+  int l2_prefetch;           // dense: K blocks of the CTA's weight slice prefetched into L2 at entry
 };
 
 
-constexpr int kGroupTile = 64;  // tokens of one expert per grouped work item (MMA N <= 64)
+// Token rows of one expert per grouped work item: up to 128 (MMA N <= 128); 64 bounds the
+// tile count that the workspace is sized for, so either size fits the same workspace.
+constexpr int kGroupTile = 64;
+constexpr int kGroupTileMax = 128;
 
 cudaError_t launch_amax(const uint16_t* x, int64_t n, float* amax_out, float* g_out, float* partial,
                         int max_partials, cudaStream_t st);
@@ -94,10 +98,11 @@ cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, co
 cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, bool grouped,
                           int grid, cudaStream_t st);
 cudaError_t launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int T, int E, int M_total, int K,
-                                int kc4, const uint8_t* sfx,
+                                int kc4, int tile_rows, const uint8_t* sfx,
                                 int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
                                 cudaStream_t st, const uint8_t* x_tok = nullptr, uint8_t* xg = nullptr);
 int stream_smem_bytes(int stages, int x_rows, int recv_bytes, bool sparse = false);
+int grouped_extra_bytes(int x_rows);  // shared memory for one tile's token indices
 int stream_recv_bytes(int M, int split);
 
 // Raises `func`'s dynamic shared-memory limit to the opt-in maximum, once per

@@ -182,6 +182,21 @@ DEVI void bulk_load_plain(void* dst, const void* src, uint32_t bytes, uint64_t* 
                : "memory");
 }
 
+// L2 prefetches: no shared memory is written and nothing completes on a barrier; a later
+// load of the same bytes finds them in L2. A prefetch returns no data, so issuing it
+// before a dependency wait cannot read stale values: the L2 is the point of coherence
+// for every later read of this GPU.
+DEVI void tma_prefetch_2d(const CUtensorMap* m, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+// `bytes` from src, both multiples of 16.
+DEVI void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Four rows (r0..r3) of a 2-D tensor whose map has a one-row box, `x` the first
 // column: 4 x box-width bytes land contiguously at dst (swizzled like a tile load).
 DEVI void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t x, int32_t r0, int32_t r1, int32_t r2,

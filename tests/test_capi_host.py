@@ -106,6 +106,13 @@ def test_tune_rejects_bad_values(lib):
     assert lib.nvfp4_tune(10, -1) == -1
     assert lib.nvfp4_tune(10, 1) == 0
     assert lib.nvfp4_tune(10, 0) == 0
+    assert lib.nvfp4_tune(14, -2) == -1  # decode L2 prefetch: -1 none, 0 all, k blocks
+    assert lib.nvfp4_tune(14, -1) == 0
+    assert lib.nvfp4_tune(14, 5) == 0
+    assert lib.nvfp4_tune(14, 0) == 0
+    assert lib.nvfp4_tune(15, 96) == -1  # grouped token tile rows: 0 (128), 64 or 128
+    assert lib.nvfp4_tune(15, 64) == 0
+    assert lib.nvfp4_tune(15, 0) == 0
 
 
 def test_sparse_sizes_match_oracle(lib):

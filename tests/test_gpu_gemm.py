@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(autouse=True)
 def _reset_tuning():
     yield
-    for key in range(1, 14):
+    for key in range(1, 16):
         m.nvfp4_tune(key, 0)
 
 
@@ -209,6 +209,47 @@ def test_weights_kept_in_l2_give_identical_results(M, split):
     kept = _run(A, B)
     assert torch.equal(kept.view(torch.int16), streamed.view(torch.int16))
     check_gemm(kept, A, B)
+
+
+@pytest.mark.parametrize("prefetch", [0, 3, -1])
+def test_l2_prefetch_sees_weights_the_previous_kernel_wrote(prefetch):
+    # A decode call prefetches its weight slice into L2 before it waits for the previous
+    # kernel in the stream (0: all of it, the default; 3: three K blocks; -1: none). Here the
+    # previous kernel is the quantiser writing the call's weights into the same buffers,
+    # alternating between two matrices inside one CUDA graph: each call must see the matrix
+    # quantised just before it, bit for bit as outside the graph.
+    M, N, K = 16, 512, 2048
+    x1, w1 = synth.dense_inputs(M, N, K, 51, 1.0, 1e-3, 0.02)
+    _, w2 = synth.dense_inputs(M, N, K, 52, 1.0, 1e-3, 0.02)
+    A, B1, B2 = Operand(x1), Operand(w1), Operand(w2)
+    wdev = [to_dev(w1), to_dev(w2)]
+    gs = [B1.dg, B2.dg]
+    wq = torch.empty_like(B1.dq)
+    sfw = torch.empty_like(B1.dsf)
+    m.nvfp4_tune(m.NVFP4_TUNE_STREAM_L2_PREFETCH, prefetch)
+
+    def step(j, out):
+        m.nvfp4_quantize(wdev[j], gs[j], q_out=wq, sf_out=sfw)
+        m.nvfp4_gemm(A.dq, A.dsf, A.dg, wq, sfw, gs[j], M, N, K, y=out)
+
+    refs = []
+    for j in range(2):
+        r = torch.empty((M, N), dtype=torch.bfloat16, device=dev())
+        step(j, r)
+        torch.cuda.synchronize()
+        assert torch.equal(wq, (B1, B2)[j].dq) and torch.equal(sfw, (B1, B2)[j].dsf)
+        refs.append(r)
+    check_gemm(refs[0], A, B1)
+    check_gemm(refs[1], A, B2)
+    outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev()) for _ in range(8)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i, o in enumerate(outs):
+            step(i % 2, o)
+    g.replay()
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        assert torch.equal(o.view(torch.int16), refs[i % 2].view(torch.int16)), i
 
 
 @pytest.mark.parametrize("pdl", [1, 2, -1])

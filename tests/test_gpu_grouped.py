@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(autouse=True)
 def _reset_tuning():
     yield
-    for key in range(1, 14):
+    for key in range(1, 16):
         m.nvfp4_tune(key, 0)
 
 
@@ -76,15 +76,31 @@ class Grouped:
         assert ok, f"grouped parity failed: worst ratio {worst}"
 
 
+@pytest.mark.parametrize("tile_rows", [0, 64])
 @pytest.mark.parametrize("counts", [
     (3, 0, 17, 1, 0, 9),                 # ragged, empty experts
     (64, 65, 63, 1, 127, 128, 129, 0),   # tile-boundary counts
+    (255, 256, 0, 257, 1),               # several 128-row tiles per expert, ragged last tiles
     (0, 0, 300, 0),                      # one expert owns every row
     (5,),                                # single expert
 ])
-def test_grouped_ragged_counts(counts):
+def test_grouped_ragged_counts(counts, tile_rows):
+    # token tiles of up to 128 rows (0: the default) or 64
+    m.nvfp4_tune(m.NVFP4_TUNE_GROUPED_TILE_ROWS, tile_rows)
     g = Grouped(counts, 256, 512, 21)
     g.check(g.run())
+
+
+def test_grouped_tile_rows_change_no_result():
+    # 64- or 128-row token tiles cut the same rows into different MMAs (N = 64 or 128
+    # token columns); every output element is the same K-ordered sum either way
+    g = Grouped((200, 0, 64, 129, 5, 300), 384, 1088, 27)
+    m.nvfp4_tune(m.NVFP4_TUNE_GROUPED_TILE_ROWS, 64)
+    y64 = g.run().clone()
+    m.nvfp4_tune(m.NVFP4_TUNE_GROUPED_TILE_ROWS, 128)
+    y128 = g.run()
+    assert torch.equal(y64.view(torch.int16), y128.view(torch.int16))
+    g.check(y128)
 
 
 def test_grouped_many_experts():
@@ -177,12 +193,14 @@ def test_grouped_bad_offsets_reported_and_output_untouched():
     assert st.item() == -8
 
 
+@pytest.mark.parametrize("tile_rows", [0, 64])
 @pytest.mark.parametrize("counts,N_gu,K", [
     ((3, 0, 17, 1, 0, 9), 256, 512),           # ragged, empty experts
     ((64, 65, 1, 127, 0), 136, 1088),          # tile-boundary counts, N_gu not a multiple of 128
-    ((0, 200, 0), 512, 256),                   # one expert, several token tiles
+    ((0, 300, 0), 512, 256),                   # one expert, several token tiles
 ])
-def test_grouped_swiglu_matches_oracle(counts, N_gu, K):
+def test_grouped_swiglu_matches_oracle(counts, N_gu, K, tile_rows):
+    m.nvfp4_tune(m.NVFP4_TUNE_GROUPED_TILE_ROWS, tile_rows)
     g = Grouped(counts, N_gu, K, 31)
     y = g.run_swiglu()
     assert tuple(y.shape) == (g.Mt, N_gu // 2)
@@ -236,6 +254,7 @@ def _gather_ws(copy, E, Mt, N, K):
 @pytest.mark.parametrize("T,counts,N,K", [
     (37, (3, 0, 17, 1, 0, 9), 256, 512),
     (200, (64, 65, 1, 70, 0), 136, 1088),
+    (300, (130, 0, 255, 2), 256, 512),     # 128-row tiles: all four token indices per lane
     (5, (40,), 256, 256),                  # more routed rows than tokens: tokens repeat
 ])
 def test_grouped_gather_matches_gathered_plain_and_oracle(T, counts, N, K, copy):

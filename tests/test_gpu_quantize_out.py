@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 def _reset_tuning():
     m.nvfp4_tune(m.NVFP4_TUNE_STREAM_MAX_M, -1)  # the plain GEMM takes the same CTA-pair kernel
     yield
-    for key in range(1, 14):
+    for key in range(1, 16):
         m.nvfp4_tune(key, 0)
 
 

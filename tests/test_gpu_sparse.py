@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(autouse=True)
 def _reset_tuning():
     yield
-    for key in range(1, 14):
+    for key in range(1, 16):
         m.nvfp4_tune(key, 0)
 
 
@@ -177,13 +177,15 @@ class GroupedSparse:
         assert ok, f"grouped sparse parity failed: worst ratio {worst}"
 
 
+@pytest.mark.parametrize("tile_rows", [0, 64])
 @pytest.mark.parametrize("counts,N,K", [
     ((3, 0, 17, 1, 0, 9), 256, 512),
     ((64, 65, 63, 1, 127, 128, 129, 0), 136, 1024),
     ((0, 300, 0), 128, 640),
     ((5,), 8, 128),
 ])
-def test_grouped_sparse_matches_oracle(counts, N, K):
+def test_grouped_sparse_matches_oracle(counts, N, K, tile_rows):
+    m.nvfp4_tune(m.NVFP4_TUNE_GROUPED_TILE_ROWS, tile_rows)
     g = GroupedSparse(counts, N, K, 91)
     g.check(g.run())
 

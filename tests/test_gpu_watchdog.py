@@ -22,7 +22,7 @@ LIMIT_US = 20_000  # 20 ms
 @pytest.fixture(autouse=True)
 def _reset_tuning():
     yield
-    for key in range(1, 14):
+    for key in range(1, 16):
         m.nvfp4_tune(key, 0)
     torch.cuda.synchronize()
 
