@@ -50,7 +50,12 @@ def _quantize_and_compare(xb, g_fixed=None):
     amax, g = m.nvfp4_amax(x)
     if g_fixed is not None:
         g = torch.tensor([g_fixed], dtype=torch.float32, device=dev())
-    q, sf = m.nvfp4_quantize(x, g)
+    # outputs start as garbage: every code byte and every scale byte, the padding rows'
+    # included (written 0), must be written
+    M, K = xb.shape
+    q = torch.full((M, K // 2), 0xAB, dtype=torch.uint8, device=dev())
+    sf = torch.full((m.nvfp4_scale_bytes(M, K),), 0xAB, dtype=torch.uint8, device=dev())
+    m.nvfp4_quantize(x, g, q_out=q, sf_out=sf)
     qo, sfo, go = oracle.quantize(xb, g_fixed)
     torch.cuda.synchronize()
     assert np.float32(amax.item()) == np.float32(oracle.amax(xb))
@@ -112,6 +117,22 @@ def test_quantize_extreme_global_scales_bit_exact(g):
     # subnormal (all codes zero): the quotients leave the fast path's exact range
     xb = synth.normal_bf16((256, 512), 10, 1.0, 1e-2)
     _quantize_and_compare(xb, np.float32(g))
+
+
+@pytest.mark.parametrize("n", [1, 7, 9, 2047, 8 * 1024 * 37 + 5, 33554432 + 3])
+def test_amax_any_length_bit_exact(n):
+    # every CTA sweeps one contiguous range of 16-byte vectors; the last CTA also takes the
+    # elements past the last whole vector. The largest |x| sits in the scalar tail, at a
+    # range boundary and at the start in turn.
+    xb = synth.normal_bf16((n,), 71, 1.0, 1e-3)
+    big = np.array([0x4480], dtype=np.uint16)  # 1024.0, above every drawn value
+    for pos in {n - 1, (n // 8) * 8 - 1 if n >= 8 else 0, 0}:
+        xi = xb.copy()
+        xi[pos] = big[0] | (0x8000 if pos % 2 else 0)  # either sign
+        amax, g = m.nvfp4_amax(to_dev(xi))
+        torch.cuda.synchronize()
+        assert np.float32(amax.item()) == np.float32(oracle.amax(xi)) == np.float32(1024.0)
+        assert np.float32(g.item()) == oracle.global_scale(oracle.amax(xi))
 
 
 def test_amax_zero_tensor_gives_unit_scale():
