@@ -565,6 +565,7 @@ def run_breakdown(m, synth, dev, stream, to_dev, quantize_dev, peaks, fp4_peak, 
     hbm = peaks["hbm"]
     if only in (None, "decode"):
         run_decode(m, synth, dev, stream, to_dev, quantize_dev, hbm, out)
+        run_decode_batched(m, synth, dev, stream, to_dev, quantize_dev, hbm, out)
     if only in (None, "decode", "sparse"):
         run_decode_sparse(m, synth, dev, stream, to_dev, hbm, out)
     if only in (None, "moe"):
@@ -630,6 +631,33 @@ def run_decode(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
                 "timing": "CUDA graph of 8 steps; a step = hot-weight call + 4 calls on rotating copies; "
                           "hot-call time = step time - cold-only step time",
                 "note": "kept: hot weight loaded L2 evict_last (NVFP4_TUNE_WEIGHT_L2=1), cold ones evict_first"}
+    del copies, wq, sfw
+
+
+def run_decode_batched(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
+    """Eight independent decode GEMMs (N = K = 8192, M rows each, their own inputs and
+    outputs) in one nvfp4_gemm_batched launch; two rotating sets of eight weight copies
+    (604 MB > L2); graph of 6 launches. GB/s of the eight matrices' packed weights + scales."""
+    import torch
+    E = 8
+    w_bits = synth.normal_bf16((SQ, SQ), 2 * 2 + 1, 0.02)
+    wq, sfw, gw = quantize_dev(to_dev(w_bits))
+    del w_bits
+    copies = [(wq.clone(), sfw.clone()) for _ in range(2 * E)]
+    wbytes = E * (wq.numel() + sfw.numel())
+    for M in (1, 16, 32):
+        xs = [quantize_dev(to_dev(synth.normal_bf16((M, SQ), 2 * 2 + 100 + e, 1.0, 1e-3))) for e in range(E)]
+        ys = [torch.empty((M, SQ), dtype=torch.bfloat16, device=dev) for _ in range(E)]
+        fn = lambda i: m.nvfp4_gemm_batched([(xs[e][0], xs[e][1], xs[e][2], copies[(i % 2) * E + e][0],
+                                              copies[(i % 2) * E + e][1], gw, ys[e]) for e in range(E)], M)
+        ms = time_graph(fn, 6, 10, stream)
+        gbs = wbytes / (ms * 1e-3) / 1e9
+        single = out.get(f"decode_M{M}")
+        out[f"decode_batched_M{M}"] = {
+            "us": ms * 1e3, "us_per_matrix": ms * 1e3 / E, "weight_GBps": gbs, "hbm_frac": gbs / hbm,
+            "hbm_frac_vs_8TBps": gbs / NOMINAL_HBM_GBS, "bytes": wbytes, "matrices": E,
+            "speedup_vs_single_calls": single["us"] * E / (ms * 1e3) if single else None,
+            "timing": "CUDA graph of 6 launches over 2 sets of 8 weight copies"}
     del copies, wq, sfw
 
 

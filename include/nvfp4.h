@@ -301,6 +301,40 @@ int nvfp4_grouped_gemm_noalloc(const uint8_t* a, const uint8_t* sfa, const float
                                void* stream);
 
 /*
+ * Several independent decode-M GEMMs in one launch: y_g = x_g @ W_g^T for g < count, every
+ * problem as nvfp4_gemm computes it ("NVFP4 linear layer", kernelindex, operation header),
+ * sharing M (1..128, the decode range: the weight-streaming kernel) but with its own
+ * operands, N and K. One launch streams all the weights, so the fixed costs of a decode
+ * call (launch, first-load latency, split-K reduction, tail) are paid once and overlap
+ * other problems' streaming, instead of once per GEMM ("The Moment of Recalibration", The
+ * Immediate Reckoning: small-M GEMMs far below the part's rates). Each problem's outputs are
+ * within the GEMM tolerance of the oracle; the split-K cluster size is chosen for the whole
+ * launch, so a problem's result may differ in the last bf16 place from a single
+ * nvfp4_gemm call of it (bit for bit equal when both use the same split).
+ *   problems  host array [count], read during the call only; every pointer a device address
+ *             as for nvfp4_gemm (a [M, K/2], sfa, ga [1], b [N, K/2], sfb, gb [1], y [M, N])
+ *   count     1..NVFP4_MAX_BATCH
+ * Returns NVFP4_ERR_INVALID_ARG (no problems, count out of range, M < 0, a null pointer),
+ * NVFP4_ERR_UNSUPPORTED_SHAPE (M > 128, or a shape nvfp4_gemm rejects),
+ * NVFP4_ERR_ALIGNMENT, or NVFP4_OK (nothing launched when M == 0). dev_status as for
+ * nvfp4_gemm (NVFP4_ERR_TIMEOUT when a pipeline wait gave up).
+ */
+#define NVFP4_MAX_BATCH 8
+typedef struct nvfp4_gemm_problem {
+  const uint8_t* a;
+  const uint8_t* sfa;
+  const float* ga;
+  const uint8_t* b;
+  const uint8_t* sfb;
+  const float* gb;
+  uint16_t* y;
+  int64_t N;
+  int64_t K;
+} nvfp4_gemm_problem;
+int nvfp4_gemm_batched(const nvfp4_gemm_problem* problems, int32_t count, int64_t M, int32_t* dev_status,
+                       void* stream);
+
+/*
  * Elementwise device encoders used by the quantiser, for exhaustive checks:
  * fp32 -> E2M1 code (round to nearest even, saturating, sign kept) and
  * fp32 -> E4M3FN code (round to nearest even, saturating to +-448).
@@ -350,9 +384,12 @@ int nvfp4_encode_e4m3(const float* v, int64_t n, uint8_t* out, void* stream);
  *                              default, 2 s). Applies to the launches that follow.
  *   NVFP4_TUNE_STREAM_L2_PREFETCH  decode-M kernels: K blocks (of 256 K elements, 512 when
  *                              sparse) of each CTA's weight slice prefetched into L2 when the
- *                              CTA starts, ahead of the launch-dependency wait. 0 (default): the
- *                              whole slice; -1: none. A prefetch moves no data into the kernel,
- *                              so results and stream order are unchanged.
+ *                              CTA starts, ahead of the launch-dependency wait. 0 (default): as
+ *                              many as keep the prefetches of all resident CTAs within 48 MB
+ *                              of L2 (the whole slice for one N = K = 8192 call), none under
+ *                              NVFP4_TUNE_PDL = 1 (the first ring is then requested early); -1: none;
+ *                              k > 0: k blocks. A prefetch moves no data into the kernel, so
+ *                              results and stream order are unchanged.
  *   NVFP4_TUNE_GROUPED_TILE_ROWS  token rows of one expert per grouped work item: 128 (the
  *                              default) or 64. An expert with r routed rows streams its weights
  *                              ceil(r / tile rows) times. Results are unchanged.

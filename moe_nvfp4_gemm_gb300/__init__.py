@@ -46,7 +46,7 @@ EXPORTS = ["nvfp4_status_string", "nvfp4_scale_bytes", "nvfp4_amax_workspace_byt
            "nvfp4_encode_e2m1",
            "nvfp4_encode_e4m3", "nvfp4_tune", "nvfp4_last_launch_count",
            "nvfp4_sparse_meta_bytes", "nvfp4_scale_bytes_b32", "nvfp4_prune_pairs", "nvfp4_quantize_b32",
-           "nvfp4_sparse_gemm", "nvfp4_grouped_sparse_gemm"]
+           "nvfp4_sparse_gemm", "nvfp4_grouped_sparse_gemm", "nvfp4_gemm_batched"]
 
 
 class NVFP4Error(RuntimeError):
@@ -62,6 +62,15 @@ _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
 _i32 = ctypes.c_int32
 _sz = ctypes.c_size_t
+
+NVFP4_MAX_BATCH = 8
+
+
+class GemmProblem(ctypes.Structure):
+    """One problem of nvfp4_gemm_batched (the C struct nvfp4_gemm_problem)."""
+    _fields_ = [("a", ctypes.c_void_p), ("sfa", ctypes.c_void_p), ("ga", ctypes.c_void_p),
+                ("b", ctypes.c_void_p), ("sfb", ctypes.c_void_p), ("gb", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
 def lib():
@@ -111,6 +120,7 @@ def lib():
             L.nvfp4_sparse_gemm.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]
             L.nvfp4_grouped_sparse_gemm.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64,
                                                     _i64, _vp, _vp, _sz, _vp, _vp]
+            L.nvfp4_gemm_batched.argtypes = [_vp, _i32, _i64, _vp, _vp]
             L.nvfp4_last_launch_count.restype = ctypes.c_int
             _lib = L
     return _lib
@@ -348,6 +358,22 @@ def nvfp4_quantize_b32(x: torch.Tensor, global_scale: torch.Tensor, q_out=None, 
     _check("nvfp4_quantize_b32", lib().nvfp4_quantize_b32(_ptr(x), M, K, _ptr(global_scale), _ptr(q_out),
                                                           _ptr(sf_out), _stream(stream)))
     return q_out, sf_out
+
+
+def nvfp4_gemm_batched(problems, M: int, dev_status=None, stream=None):
+    """Several decode-M GEMMs in one launch. problems: sequence of (a, sfa, ga, b, sfb, gb, y)
+    tuples of CUDA tensors (y bf16 [M, N], preallocated); N and K come from b and a."""
+    arr = (GemmProblem * max(1, len(problems)))()
+    for i, (a, sfa, ga, b, sfb, gb, y) in enumerate(problems):
+        for t, n in ((a, "a"), (sfa, "sfa"), (b, "b"), (sfb, "sfb")):
+            _cuda(t, torch.uint8, n)
+        _cuda(ga, torch.float32, "ga")
+        _cuda(gb, torch.float32, "gb")
+        _cuda(y, torch.bfloat16, "y")
+        arr[i] = GemmProblem(a.data_ptr(), sfa.data_ptr(), ga.data_ptr(), b.data_ptr(), sfb.data_ptr(),
+                             gb.data_ptr(), y.data_ptr(), b.shape[0], 2 * b.shape[1])
+    _check("nvfp4_gemm_batched", lib().nvfp4_gemm_batched(ctypes.cast(arr, ctypes.c_void_p), len(problems), M,
+                                                          _ptr(dev_status), _stream(stream)))
 
 
 def nvfp4_sparse_gemm(a, sfa, ga, b_c, sfb_c, meta, gb, M: int, N: int, K: int, y=None, dev_status=None,

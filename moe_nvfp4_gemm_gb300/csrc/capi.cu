@@ -141,8 +141,21 @@ int stream_pdl_mode() { return g_tune.pdl == 0 ? 2 : (g_tune.pdl < 0 ? 0 : g_tun
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
 
-// K blocks of each decode CTA's weight slice prefetched into L2 at entry (all of them by default).
-int stream_l2_prefetch() { return g_tune.stream_l2_prefetch == 0 ? (1 << 20) : (g_tune.stream_l2_prefetch < 0 ? 0 : g_tune.stream_l2_prefetch); }
+// K blocks of each decode CTA's weight slice prefetched into L2 at entry. By default as many
+// as keep the prefetches of all resident CTAs (two per SM) within 48 MB of the 126 MB L2:
+// the whole slice of one N = K = 8192 call (37.7 MB), but only part of each slice when a
+// batched launch's resident CTAs stream far more, where prefetching everything would evict
+// prefetched lines before their loads (measured: 8 batched N = K = 8192 GEMMs, M = 1,
+// 7.16 us per matrix with whole slices, 6.31 us without prefetch, 6.35 us with 8 blocks).
+// With the weights requested before the launch dependency (NVFP4_TUNE_PDL = 1) the first
+// ring already overlaps the previous kernel, and prefetching the rest measured slower
+// (9.7 against 8.5 us at M = 1): none by default then.
+int stream_l2_prefetch(int64_t grid, int sms, int64_t block_bytes) {
+  if (g_tune.stream_l2_prefetch != 0) return g_tune.stream_l2_prefetch < 0 ? 0 : g_tune.stream_l2_prefetch;
+  if (stream_pdl_mode() == 1) return 0;
+  const int64_t resident = grid < 2 * sms ? grid : 2 * int64_t(sms);
+  return static_cast<int>((int64_t(48) << 20) / (resident * block_bytes));
+}
 uint64_t watchdog_ns() { return g_tune.watchdog_us ? uint64_t(g_tune.watchdog_us) * 1000u : kWatchdogNs; }
 
 int64_t pad16(int64_t v) { return (v + 15) / 16 * 16; }
@@ -366,7 +379,7 @@ int nvfp4_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, const uint
     s.w_keep = g_tune.weight_l2;
     s.watchdog_ns = watchdog_ns();
     s.drop_stage = g_tune.withhold_stage;
-    s.l2_prefetch = stream_l2_prefetch();
+    s.l2_prefetch = stream_l2_prefetch(int64_t(NT) * split, d.sms, 16384 + 2048);
     const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0) - 1536;
     const int recv_bytes = stream_recv_bytes(s.M, split);
     int stages = g_tune.stream_stages;
@@ -562,7 +575,7 @@ int nvfp4_sparse_gemm(const uint8_t* a, const uint8_t* sfa, const float* ga, con
     s.w_keep = g_tune.weight_l2;
     s.watchdog_ns = watchdog_ns();
     s.drop_stage = g_tune.withhold_stage;
-    s.l2_prefetch = stream_l2_prefetch();
+    s.l2_prefetch = stream_l2_prefetch(int64_t(NT) * split, d.sms, 16384 + 2048 + 4096);
     const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0, true) - 1536;
     const int recv_bytes = stream_recv_bytes(s.M, split);
     int stages = g_tune.stream_stages;
@@ -589,6 +602,95 @@ static int64_t grouped_max_tiles(int32_t E, int64_t M_total) { return (M_total +
 
 static int64_t grouped_slab_offset(int32_t E, int64_t M_total) {
   return (16 + grouped_max_tiles(E, M_total) * 16 + 255) / 256 * 256;
+}
+
+int nvfp4_gemm_batched(const nvfp4_gemm_problem* problems, int32_t count, int64_t M, int32_t* dev_status,
+                       void* stream) {
+  g_last_launches = 0;
+  if (!problems || count < 1 || count > NVFP4_MAX_BATCH || M < 0) return NVFP4_ERR_INVALID_ARG;
+  for (int g = 0; g < count; ++g) {
+    const int rc = check_gemm_shape(M, problems[g].N, problems[g].K);
+    if (rc) return rc;
+  }
+  if (M > 128) return NVFP4_ERR_UNSUPPORTED_SHAPE;  // the weight-streaming kernel's token range
+  if (M == 0) return NVFP4_OK;
+  for (int g = 0; g < count; ++g) {
+    const nvfp4_gemm_problem& q = problems[g];
+    if (!q.a || !q.sfa || !q.ga || !q.b || !q.sfb || !q.gb || !q.y) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned16(q.a) || !aligned16(q.sfa) || !aligned16(q.b) || !aligned16(q.sfb) || !aligned16(q.y))
+      return NVFP4_ERR_ALIGNMENT;
+  }
+  DevInfo d;
+  int rc = device_info(d);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  // One split-K cluster size for the launch, chosen from all GEMMs' 128-row weight tiles
+  // as a single call chooses it from its own; no GEMM splits finer than its K blocks.
+  int64_t tiles = 0;
+  int min_kb = 1 << 30;
+  for (int g = 0; g < count; ++g) {
+    tiles += (problems[g].N + 127) / 128;
+    const int kb = static_cast<int>((problems[g].K + 255) / 256);
+    if (kb < min_kb) min_kb = kb;
+  }
+  int split = g_tune.stream_split;
+  if (split == 0) {
+    const int64_t sp = (2 * static_cast<int64_t>(d.sms)) / tiles;
+    split = static_cast<int>(sp < 1 ? 1 : (sp > 8 ? 8 : sp));
+  }
+  if (split > min_kb) split = min_kb;
+  if (tiles * split > (int64_t(1) << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+
+  BatchParams bp = {};  // kernel parameters: copied by the launch
+  int cta = 0;
+  for (int g = 0; g < count; ++g) {
+    const nvfp4_gemm_problem& q = problems[g];
+    if ((rc = encode_2d(&bp.w[g], q.b, q.N, q.K / 2, 128))) return rc;
+    if ((rc = encode_2d(&bp.x[g], q.a, M, q.K / 2, 16))) return rc;
+    bp.sfw[g] = q.sfb;
+    bp.sfx[g] = q.sfa;
+    bp.ga[g] = q.ga;
+    bp.gb[g] = q.gb;
+    bp.y[g] = q.y;
+    bp.N[g] = static_cast<int>(q.N);
+    bp.K[g] = static_cast<int>(q.K);
+    bp.cta_base[g] = cta;
+    cta += static_cast<int>((q.N + 127) / 128) * split;
+  }
+  bp.cta_base[count] = cta;
+  bp.count = count;
+
+  StreamArgs s = {};
+  s.sfw_stride = 0;
+  s.status = dev_status;
+  s.M = static_cast<int>(M);
+  s.x_rows = static_cast<int>(pad16(M));
+  s.acc_cols = (s.x_rows + 31) / 32 * 32;
+  s.acc_bufs = 1;
+  s.split = split;
+  s.pdl = stream_pdl_mode();
+  s.w_keep = g_tune.weight_l2;
+  s.watchdog_ns = watchdog_ns();
+  s.drop_stage = g_tune.withhold_stage;
+  s.l2_prefetch = stream_l2_prefetch(cta, d.sms, 16384 + 2048);
+  const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0) - 1536;
+  const int recv_bytes = stream_recv_bytes(s.M, split);
+  int stages = g_tune.stream_stages;
+  if (stages == 0) {
+    stages = (110 * 1024 - 1536 - recv_bytes) / stage_bytes;  // two CTAs per SM
+    const int tmem_room = (256 - s.acc_cols) / 32;
+    if (stages > tmem_room) stages = tmem_room;
+    if (stages < 2) stages = 2;
+  }
+  while (split > 1 && stages * stage_bytes < recv_bytes) ++stages;
+  if (stream_smem_bytes(stages, s.x_rows, recv_bytes) > kSmemLimit) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  s.stages = stages;
+  s.tmem_cols = pow2_at_least(s.acc_cols + 32 * stages);
+  if (s.tmem_cols > 512) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  rc = from_cuda(launch_batched(bp, s, cta, st));
+  g_last_launches = 1;
+  return rc;
 }
 
 size_t nvfp4_grouped_gemm_workspace_bytes(int32_t E, int64_t M_total, int64_t N, int64_t K) {

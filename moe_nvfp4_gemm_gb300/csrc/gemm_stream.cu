@@ -95,10 +95,10 @@ constexpr uint32_t kStreamEpilogueBarrier = 2;  // the 4 epilogue warps
 // bit 2 pair-wise 2:4 sparse weights (dense or plain grouped path): the weight tile holds compressed
 // values, a stage spans 512 K elements (four K = 128 sparse MMAs) and carries the metadata
 // tile. Compiled separately so that the plain kernels carry none of them.
-template <bool GROUPED, int VARIANT = 0>
-__global__ void __launch_bounds__(kStreamThreads, 2)
-    k_gemm_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                  const StreamArgs p) {
+// The kernel body; `cta` is this CTA's index among the CTAs of its problem (blockIdx.x
+// for a single GEMM or the grouped kernel, the index within its GEMM in a batched launch).
+template <bool GROUPED, int VARIANT>
+DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& p, const int cta) {
   constexpr bool SPARSE = (VARIANT & 4) != 0;
   constexpr int KSTAGE = SPARSE ? 512 : 256;  // K elements per stage
   constexpr int KMMA = KSTAGE / 4;            // K elements per MMA
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   Item first_it;
   int n_pre = 0;
   if (!GROUPED) {
-    get_item<false>(p, blockIdx.x, NT * p.split, NT, KB, first_it);
+    get_item<false>(p, cta, NT * p.split, NT, KB, first_it);
     n_pre = min(STAGES, first_it.kb1 - first_it.kb0);
   }
 
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     }
     if (p.pdl == 2) griddep_wait();  // set-up-only overlap: no load before the previous kernel completes
     for (int j = 0; j < n_pre; ++j)
-      if (!(blockIdx.x == 0 && j + 1 == p.drop_stage))  // test hook: stage withheld
+      if (!(cta == 0 && j + 1 == p.drop_stage))  // test hook: stage withheld
         issue_stage(j, first_it.kb0 + j, src, p.pdl != 1, p.w_keep != 0, keep, keep);
   }
   if (warp == 1) {
@@ -280,11 +280,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   int n_items, first, stride;
   if (GROUPED) {
     n_items = __ldg(p.n_tiles) * NT;
-    first = blockIdx.x;
+    first = cta;
     stride = gridDim.x;
   } else {
     n_items = NT * p.split;
-    first = blockIdx.x;
+    first = cta;
     stride = n_items;  // one item per CTA
   }
   const uint32_t sf_base = tmem + p.acc_bufs * p.acc_cols;
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         }
         const bool pre = issued < n_pre;  // requested in the prologue
         ++issued;
-        const bool withheld = blockIdx.x == 0 && issued == p.drop_stage;  // test hook
+        const bool withheld = cta == 0 && issued == p.drop_stage;  // test hook
         if (!pre && !withheld && elect_one()) issue_stage(s, kb, src, !pending, have_pol, pol_w, pol_x);
         __syncwarp();
         if (pending) {
@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     if (mine > 0 && !received) *abort_flag = 1;
     if (received && !*abort_flag) {
       const int q = warp & 3;
-      const int wrow = (blockIdx.x / S) * 128 + q * 32 + lane;
+      const int wrow = (cta / S) * 128 + q * 32 + lane;
       const float alpha = dense_alpha;
       for (int idx = 0; idx < mine; ++idx) {
         float v = 0.0f;
@@ -604,6 +604,33 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     tmem_dealloc(tmem, p.tmem_cols);
   }
   if (threadIdx.x == 0 && *abort_flag) report_status(p.status, kStatusTimeout);
+}
+
+template <bool GROUPED, int VARIANT = 0>
+__global__ void __launch_bounds__(kStreamThreads, 2)
+    k_gemm_stream(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                  const StreamArgs p) {
+  stream_body<GROUPED, VARIANT>(tmW, tmX, p, static_cast<int>(blockIdx.x));
+}
+
+// Several independent decode-M GEMMs in one launch (same M, their own weights, inputs,
+// outputs, N and K): CTAs [cta_base[g], cta_base[g + 1]) run GEMM g exactly as a single
+// call's grid would, with the launch's split-K cluster size (every GEMM's CTA count is a
+// multiple of it, so no cluster spans two GEMMs).
+__global__ void __launch_bounds__(kStreamThreads, 2)
+    k_gemm_batched(const __grid_constant__ BatchParams bp, const __grid_constant__ StreamArgs p) {
+  const int b = static_cast<int>(blockIdx.x);
+  int g = 0;
+  while (g + 1 < bp.count && b >= bp.cta_base[g + 1]) ++g;
+  StreamArgs q = p;
+  q.sfw = bp.sfw[g];
+  q.sfx = bp.sfx[g];
+  q.ga = bp.ga[g];
+  q.gb = bp.gb[g];
+  q.y = bp.y[g];
+  q.N = bp.N[g];
+  q.K = bp.K[g];
+  stream_body<false, 0>(bp.w[g], bp.x[g], q, b - bp.cta_base[g]);
 }
 
 // ---- grouped preparation ------------------------------------------------------------
@@ -758,6 +785,34 @@ int grouped_extra_bytes(int x_rows) { return x_rows * 4 > 256 ? x_rows * 4 : 256
 
 int stream_smem_bytes(int stages, int x_rows, int recv_bytes, bool sparse) {
   return stages * StreamLayout(x_rows, sparse).stage_bytes + recv_bytes + 1024 + 512;
+}
+
+cudaError_t launch_batched(const BatchParams& bp, const StreamArgs& a, int grid, cudaStream_t st) {
+  const int smem = stream_smem_bytes(a.stages, a.x_rows, stream_recv_bytes(a.M, a.split));
+  cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_gemm_batched));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kStreamThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int nattr = 0;
+  if (a.split > 1) {
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = a.split;
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
+  }
+  if (a.pdl) {
+    attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+    ++nattr;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = nattr;
+  return cudaLaunchKernelEx(&cfg, k_gemm_batched, bp, a);
 }
 
 cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, bool grouped, int grid,

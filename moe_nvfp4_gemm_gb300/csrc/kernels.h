@@ -76,6 +76,23 @@ struct StreamArgs {
 };
 
 
+// A batched decode launch: up to kMaxBatch GEMMs sharing M (and the launch's split-K,
+// stage count and token rows); tensor maps and pointers per GEMM, passed as kernel
+// parameters.
+constexpr int kMaxBatch = 8;
+struct BatchParams {
+  CUtensorMap w[kMaxBatch];  // weights [N, K/2], 128-row boxes
+  CUtensorMap x[kMaxBatch];  // activations [M, K/2], 16-row boxes
+  const uint8_t* sfw[kMaxBatch];
+  const uint8_t* sfx[kMaxBatch];
+  const float* ga[kMaxBatch];
+  const float* gb[kMaxBatch];
+  uint16_t* y[kMaxBatch];
+  int N[kMaxBatch], K[kMaxBatch];
+  int cta_base[kMaxBatch + 1];  // first CTA of each GEMM; cta_base[count] = grid
+  int count;
+};
+
 // Token rows of one expert per grouped work item: up to 128 (MMA N <= 128); 64 bounds the
 // tile count that the workspace is sized for, so either size fits the same workspace.
 constexpr int kGroupTile = 64;
@@ -97,6 +114,7 @@ cudaError_t launch_dense_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, co
                               cudaStream_t st, bool quantized_out = false);
 cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, bool grouped,
                           int grid, cudaStream_t st);
+cudaError_t launch_batched(const BatchParams& bp, const StreamArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_grouped_prep(const int32_t* offsets, const int32_t* row_token, int T, int E, int M_total, int K,
                                 int kc4, int tile_rows, const uint8_t* sfx,
                                 int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,

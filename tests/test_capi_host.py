@@ -134,3 +134,23 @@ def test_sparse_host_validation(lib):
     assert pr(0, 128) == 0 and pr(4, 64) == -2 and pr(4, 128, w=0) == -1 and pr(4, 128, w=8) == -3
     qb = lambda M, K, x=16: lib.nvfp4_quantize_b32(P(x), M, K, P(16), P(16), P(16), None)
     assert qb(0, 128) == 0 and qb(4, 64) == -2 and qb(4, 128, x=0) == -1 and qb(4, 128, x=24) == -3
+
+
+def _batched(lib, problems, count, M):
+    import moe_nvfp4_gemm_gb300 as m
+    arr = (m.GemmProblem * max(1, len(problems)))(*problems)
+    return lib.nvfp4_gemm_batched(ctypes.cast(arr, P), count, M, None, None)
+
+
+def test_gemm_batched_host_validation(lib):
+    import moe_nvfp4_gemm_gb300 as m
+    ok = m.GemmProblem(16, 16, 16, 16, 16, 16, 16, 256, 512)
+    assert lib.nvfp4_gemm_batched(None, 1, 4, None, None) == -1   # no problems
+    assert _batched(lib, [ok], 0, 4) == -1                         # count out of range
+    assert _batched(lib, [ok] * 9, 9, 4) == -1
+    assert _batched(lib, [ok], 1, -1) == -1                        # negative M
+    assert _batched(lib, [ok], 1, 129) == -2                       # above the decode range
+    assert _batched(lib, [ok], 1, 0) == 0                          # empty M: nothing to do
+    assert _batched(lib, [ok, m.GemmProblem(16, 16, 16, 16, 16, 16, 16, 256, 100)], 2, 4) == -2  # K % 64
+    assert _batched(lib, [ok, m.GemmProblem(16, 16, 16, 0, 16, 16, 16, 256, 512)], 2, 4) == -1   # null b
+    assert _batched(lib, [ok, m.GemmProblem(16, 16, 16, 24, 16, 16, 16, 256, 512)], 2, 4) == -3  # misaligned b

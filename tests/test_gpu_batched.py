@@ -1,0 +1,96 @@
+"""GPU parity of the batched decode GEMM (nvfp4_gemm_batched): several independent
+problems sharing M, each with its own operands, N and K, in one launch. Every problem's
+output is compared with the oracle's GEMM of that problem, element by element:
+|y - y_ref| <= 4e-3 |y_ref| + 1e-5 sum_k |x^_k w^_k| ("NVFP4 linear layer", kernelindex,
+operation header: y = x @ W^T per problem)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_nvfp4_gemm_gb300 as m
+from tests.helpers import Operand, check_gemm, dev
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _reset_tuning():
+    yield
+    for key in range(1, 16):
+        m.nvfp4_tune(key, 0)
+
+
+def _problems(M, shapes, seed):
+    out = []
+    for i, (N, K) in enumerate(shapes):
+        x, w = synth.dense_inputs(M, N, K, seed + i, 1.0, 1e-3, 0.02)
+        out.append((Operand(x), Operand(w)))
+    return out
+
+
+def _run(M, probs, status=None):
+    ys = [torch.full((M, B.rows), float("nan"), dtype=torch.bfloat16, device=dev()) for _, B in probs]
+    m.nvfp4_gemm_batched([(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, y) for (A, B), y in zip(probs, ys)], M,
+                         dev_status=status)
+    torch.cuda.synchronize()
+    return ys
+
+
+MIXED = [(256, 512), (136, 1088), (512, 2048), (8, 64), (1032, 192)]
+
+
+@pytest.mark.parametrize("M", [1, 5, 16, 33, 128])
+def test_batched_mixed_shapes_match_oracle(M):
+    # N from one partial 128-row weight tile to several with a ragged last one, K from one
+    # partial stage to several; every output element is written (the outputs start as NaN)
+    probs = _problems(M, MIXED, 100)
+    for (A, B), y in zip(probs, _run(M, probs)):
+        check_gemm(y, A, B)
+
+
+@pytest.mark.parametrize("split", [1, 2, 4])
+def test_batched_equals_single_calls_with_the_same_split(split):
+    # the same kernel body on the same tiles: bit for bit what single calls give when both
+    # use one split-K cluster size
+    M = 16
+    probs = _problems(M, [(384, 1024), (128, 2048), (640, 512)], 200)
+    m.nvfp4_tune(m.NVFP4_TUNE_STREAM_SPLIT, split)
+    ys = _run(M, probs)
+    for (A, B), y in zip(probs, ys):
+        y1 = m.nvfp4_gemm(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, M, B.rows, A.K)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), y1.view(torch.int16))
+        check_gemm(y, A, B)
+
+
+def test_batched_eight_problems_and_status_untouched():
+    M = 32
+    probs = _problems(M, [(512 + 128 * i, 1024 + 256 * (i % 3)) for i in range(m.NVFP4_MAX_BATCH)], 300)
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    for (A, B), y in zip(probs, _run(M, probs, st)):
+        check_gemm(y, A, B)
+    assert st.item() == 0
+
+
+def test_batched_rejects_bad_batches():
+    M = 4
+    (A, B), = _problems(M, [(128, 256)], 400)
+    y = torch.empty((M, 128), dtype=torch.bfloat16, device=dev())
+    one = (A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, y)
+    with pytest.raises(m.NVFP4Error) as e:
+        m.nvfp4_gemm_batched([one] * (m.NVFP4_MAX_BATCH + 1), M)
+    assert e.value.status == -1
+    with pytest.raises(m.NVFP4Error) as e:
+        m.nvfp4_gemm_batched([one], 129)
+    assert e.value.status == -2
+
+
+def test_batched_decode_workload_sampled():
+    # four N = K = 8192 problems at M = 16 (the decode workload's shape), sampled on
+    # every 128-row weight tile's first and last rows
+    M, SQ = 16, 8192
+    probs = _problems(M, [(SQ, SQ)] * 4, 500)
+    cols = np.unique(np.concatenate([np.arange(0, SQ, 128), np.arange(127, SQ, 128)]))
+    for (A, B), y in zip(probs, _run(M, probs)):
+        check_gemm(y, A, B, cols=cols)

@@ -81,6 +81,28 @@ def test_grouped_kernel_times_out_cleanly_and_recovers(stage):
     _timed_out_then_recovers(lambda st: g.run(status=st), g.check, stage)
 
 
+@pytest.mark.parametrize("stage", [1, 2])
+def test_batched_kernel_times_out_cleanly_and_recovers(stage):
+    # the first CTA of every problem in the launch withholds the stage (a problem with fewer
+    # stages per CTA withholds nothing); split-K clusters of 4
+    from tests.test_gpu_batched import _problems
+    M = 16
+    probs = _problems(M, [(512, 2048), (256, 1024)], 45)
+    m.nvfp4_tune(m.NVFP4_TUNE_STREAM_SPLIT, 4)
+
+    def run(st):
+        ys = [torch.empty((M, B.rows), dtype=torch.bfloat16, device=dev()) for _, B in probs]
+        m.nvfp4_gemm_batched([(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, y) for (A, B), y in zip(probs, ys)], M,
+                             dev_status=st)
+        return ys
+
+    def check(ys):
+        for (A, B), y in zip(probs, ys):
+            check_gemm(y, A, B)
+
+    _timed_out_then_recovers(run, check, stage)
+
+
 def test_default_limit_is_restored():
     # with the hook off and the limit back at its default an ordinary call succeeds
     A, B = dense_case(128, 256, 512, 43)
