@@ -83,6 +83,31 @@ DEVI bool get_item(const StreamArgs& p, int i, int n_items, int NT, int KB, Item
   return true;
 }
 
+// Item i of a role's sequence (i, i + stride, ...). Grouped: `desc` holds item i's tile
+// descriptor, loaded one item ahead; after filling `it` the load for item i + stride is
+// issued into it, so that no role waits for a global load at an item boundary (a role
+// that stalls there stops freeing ring slots, and the weight stream loses requests in
+// flight).
+template <bool GROUPED>
+DEVI bool next_item(const StreamArgs& p, int i, int stride, int n_items, int NT, int KB, int4& desc, Item& it) {
+  if (!GROUPED) return get_item<false>(p, i, n_items, NT, KB, it);
+  if (i >= n_items) return false;
+  it.wt = i % NT;
+  it.e = desc.x;
+  it.row0 = desc.y;
+  it.rows = desc.z;
+  it.slab = desc.w;
+  it.kb0 = 0;
+  it.kb1 = KB;
+  if (i + stride < n_items) desc = __ldg(p.tiles + (i + stride) / NT);
+  return true;
+}
+
+template <bool GROUPED>
+DEVI int4 first_desc(const StreamArgs& p, int first, int n_items, int NT) {
+  return (GROUPED && first < n_items) ? __ldg(p.tiles + first / NT) : make_int4(0, 0, 0, 0);
+}
+
 // Warp roles: 0 TMA producer, 1 MMA issuer, 2-5 epilogue, 6 stage waiter (waits for a
 // stage's bytes and hands it to the MMA warp through a named barrier, so that the
 // MMA-issuing warp itself never waits on an mbarrier per stage).
@@ -315,7 +340,8 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
     };
     int4 tok_regs = make_int4(0, 0, 0, 0);
     bool tok_ready = false;
-    for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it) && !*abort_flag; i += stride) {
+    int4 desc = first_desc<GROUPED>(p, first, n_items, NT);
+    for (int i = first; next_item<GROUPED>(p, i, stride, n_items, NT, KB, desc, it) && !*abort_flag; i += stride) {
       const Src src = item_src(it);
       const int n16 = src.n16;
       const uint8_t* sfx = src.sfx;
@@ -383,7 +409,8 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
     uint32_t ph = 0;
     uint32_t acc_ph[2] = {0, 0};
     Item it;
-    for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it); i += stride) {
+    int4 desc = first_desc<GROUPED>(p, first, n_items, NT);
+    for (int i = first; next_item<GROUPED>(p, i, stride, n_items, NT, KB, desc, it); i += stride) {
       const bool item_ok =
           __all_sync(0xffffffffu, *abort_flag == 0) && mbar_wait_warp(&tempty[buf], acc_ph[buf] ^ 1, abort_flag, wd);
       acc_ph[buf] ^= 1;
@@ -401,7 +428,8 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
   } else if (warp == 1) {
     int s = 0, buf = 0;
     Item it;
-    for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it); i += stride) {
+    int4 desc = first_desc<GROUPED>(p, first, n_items, NT);
+    for (int i = first; next_item<GROUPED>(p, i, stride, n_items, NT, KB, desc, it); i += stride) {
       const int n_mma = ((it.rows + 15) >> 4) * 16;
       const uint32_t idesc = SPARSE ? idesc_nvf4_sp(128, n_mma) : idesc_nvf4(128, n_mma);
       const uint32_t acc = tmem + buf * p.acc_cols;
@@ -478,7 +506,8 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
     int buf = 0;
     uint32_t acc_ph[2] = {0, 0};
     Item it;
-    for (int i = first; get_item<GROUPED>(p, i, n_items, NT, KB, it); i += stride) {
+    int4 desc = first_desc<GROUPED>(p, first, n_items, NT);
+    for (int i = first; next_item<GROUPED>(p, i, stride, n_items, NT, KB, desc, it); i += stride) {
       if (!mbar_wait_warp(&tfull[buf], acc_ph[buf], abort_flag, wd)) break;
       tc_fence_after();
       const float alpha = ga * (GROUPED ? __ldg(p.gb + it.e) : gb0);
