@@ -108,11 +108,13 @@ DEVI int4 first_desc(const StreamArgs& p, int first, int n_items, int NT) {
   return (GROUPED && first < n_items) ? __ldg(p.tiles + first / NT) : make_int4(0, 0, 0, 0);
 }
 
-// Warp roles: 0 TMA producer, 1 MMA issuer, 2-5 epilogue, 6 stage waiter (waits for a
-// stage's bytes and hands it to the MMA warp through a named barrier, so that the
-// MMA-issuing warp itself never waits on an mbarrier per stage).
-constexpr int kStreamThreads = 224;
+// Warp roles: 0 TMA producer (grouped: the weight part of each stage), 1 MMA issuer, 2-5
+// epilogue, 6 stage waiter (waits for a stage's bytes and hands it to the MMA warp through
+// a named barrier, so that the MMA-issuing warp itself never waits on an mbarrier per
+// stage), 7 grouped: token producer.
+constexpr int kStreamThreads = 256;
 constexpr int kStreamWaiterWarp = 6;
+constexpr int kStreamTokenWarp = 7;  // grouped path: token rows and their scales
 constexpr uint32_t kStreamHandoffBarrier = 1;
 constexpr uint32_t kStreamEpilogueBarrier = 2;  // the 4 epilogue warps
 
@@ -200,17 +202,18 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
       bulk_load_plain(st + L.sfx_off, src.sfx + kb * 2048, nsub * 512, bar);
   };
   // Requests stage st_idx = K block kb of an item: the 128-row weight tile and its
-  // scales, and unless deferred (with_x false) the token tile and its scales.
+  // scales, and on the dense path, unless deferred (with_x false), the token tile and its
+  // scales (the grouped path's token warp requests those, issue_tokens).
   auto issue_stage = [&](int st_idx, int kb, const Src& src, bool with_x, bool hint, uint64_t pol_w,
                          uint64_t pol_x) {
     const int n16 = src.n16;
     const int32_t wrow0 = src.wrow0;
     const uint8_t* sfw = src.sfw;
-    const uint8_t* sfx = src.sfx;
     const int nsub = min(4, (K - kb * KSTAGE) / KMMA);
     uint8_t* st = smem + st_idx * L.stage_bytes;
     uint64_t* bar = &full[st_idx];
-    mbar_arrive_expect_tx(bar, 16384 + (SPARSE ? 2 : 1) * n16 * 2048 + nsub * 1024 + (SPARSE ? 4096 : 0));
+    mbar_arrive_expect_tx(bar, 16384 + nsub * 512 + (SPARSE ? 4096 : 0) +
+                                   (GROUPED ? 0 : (SPARSE ? 2 : 1) * n16 * 2048 + nsub * 512));
     if (hint) {
       tma_load_2d(st, &tmW, bar, kb * 128, wrow0, pol_w);
       bulk_load(st + L.sfw_off, sfw + kb * 2048, nsub * 512, bar, pol_w);
@@ -220,16 +223,26 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
       bulk_load_plain(st + L.sfw_off, sfw + kb * 2048, nsub * 512, bar);
       if (SPARSE) bulk_load_plain(st + L.meta_off, src.meta + kb * 4096, 4096, bar);
     }
-    if (with_x && GROUPED && (VARIANT & 2)) {
-      // token gather: four rows per instruction from the one-row-box map of x
-      for (int j = 0; j < n16 * 4; ++j)
+    if (!GROUPED && with_x) issue_x(st, bar, kb, src, hint, pol_x);
+  };
+  // Grouped path, token warp: the token rows of stage st_idx (one tile load per 16 rows, or
+  // with a token gather four rows per tile::gather4 from the one-row-box map of x) and
+  // their scales, with their own expected bytes on the stage's barrier (which counts the
+  // weight warp's and the token warp's arrivals).
+  auto issue_tokens = [&](int st_idx, int kb, const Src& src, bool hint, uint64_t pol_x) {
+    const int nsub = min(4, (K - kb * KSTAGE) / KMMA);
+    uint8_t* st = smem + st_idx * L.stage_bytes;
+    uint64_t* bar = &full[st_idx];
+    mbar_arrive_expect_tx(bar, (SPARSE ? 2 : 1) * src.n16 * 2048 + nsub * 512);
+    if (VARIANT & 2) {
+      for (int j = 0; j < src.n16 * 4; ++j)
         tma_gather4(st + L.x_off + j * 512, &tmX, bar, kb * 128, tok_idx[4 * j], tok_idx[4 * j + 1],
                     tok_idx[4 * j + 2], tok_idx[4 * j + 3]);
       if (hint)
-        bulk_load(st + L.sfx_off, sfx + kb * 2048, nsub * 512, bar, pol_x);
+        bulk_load(st + L.sfx_off, src.sfx + kb * 2048, nsub * 512, bar, pol_x);
       else
-        bulk_load_plain(st + L.sfx_off, sfx + kb * 2048, nsub * 512, bar);
-    } else if (with_x) {
+        bulk_load_plain(st + L.sfx_off, src.sfx + kb * 2048, nsub * 512, bar);
+    } else {
       issue_x(st, bar, kb, src, hint, pol_x);
     }
   };
@@ -248,7 +261,7 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
     prefetch_tmap(&tmW);  // first, so that the descriptors are fetched while the barriers are set up
     prefetch_tmap(&tmX);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], GROUPED ? 2 : 1);  // grouped: the weight warp and the token warp arrive
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -332,33 +345,9 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
     if (p.pdl == 2) griddep_wait();
     int pend_stage[16], pend_kb[16], npend = 0;
     Item it;
-    auto load_tokens = [&](const Item& x) {
-      return make_int4(__ldg(p.row_token + x.row0 + min(lane, x.rows - 1)),
-                       __ldg(p.row_token + x.row0 + min(lane + 32, x.rows - 1)),
-                       __ldg(p.row_token + x.row0 + min(lane + 64, x.rows - 1)),
-                       __ldg(p.row_token + x.row0 + min(lane + 96, x.rows - 1)));
-    };
-    int4 tok_regs = make_int4(0, 0, 0, 0);
-    bool tok_ready = false;
     int4 desc = first_desc<GROUPED>(p, first, n_items, NT);
     for (int i = first; next_item<GROUPED>(p, i, stride, n_items, NT, KB, desc, it) && !*abort_flag; i += stride) {
       const Src src = item_src(it);
-      const int n16 = src.n16;
-      const uint8_t* sfx = src.sfx;
-      if (GROUPED && (VARIANT & 2)) {
-        // this item's token rows (loaded during the previous item, four per lane); rows past
-        // the tile's count repeat its last row (their accumulator columns are never stored),
-        // indices clamped into x (prep reports bad ones)
-        if (!tok_ready) tok_regs = load_tokens(it);
-        tok_idx[lane] = min(max(tok_regs.x, 0), p.T - 1);
-        tok_idx[lane + 32] = min(max(tok_regs.y, 0), p.T - 1);
-        tok_idx[lane + 64] = min(max(tok_regs.z, 0), p.T - 1);
-        tok_idx[lane + 96] = min(max(tok_regs.w, 0), p.T - 1);
-        __syncwarp();
-        Item nx;  // start the next item's index loads now; they land while this item streams
-        tok_ready = get_item<GROUPED>(p, i + stride, n_items, NT, KB, nx);
-        if (tok_ready) tok_regs = load_tokens(nx);
-      }
       for (int kb = it.kb0; kb < it.kb1; ++kb) {
         if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag, wd)) break;
         if (!have_pol && issued >= STAGES && *policies_ready) {
@@ -399,6 +388,70 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
         volatile int32_t dummy = 0;
         mbar_wait_warp(&full[i], issued_phase[i], &dummy, wd);
       }
+  } else if (warp == kStreamTokenWarp) {
+    // Grouped path: requests every stage's token rows and their scales, in the weight warp's
+    // item and stage order (two warps issue a stage's copies in about half the time one
+    // does; with one, the issuing thread limited each CTA's weight stream). Dense path: idle.
+    if (GROUPED) {
+      uint64_t pol_x = 0;
+      bool have_pol = false;
+      int issued = 0;
+      int s = 0;
+      uint32_t ph = 0;
+      int issued_phase[16];
+      for (int j = 0; j < 16; ++j) issued_phase[j] = -1;
+      Item it;
+      auto load_tokens = [&](const Item& x) {
+        return make_int4(__ldg(p.row_token + x.row0 + min(lane, x.rows - 1)),
+                         __ldg(p.row_token + x.row0 + min(lane + 32, x.rows - 1)),
+                         __ldg(p.row_token + x.row0 + min(lane + 64, x.rows - 1)),
+                         __ldg(p.row_token + x.row0 + min(lane + 96, x.rows - 1)));
+      };
+      int4 tok_regs = make_int4(0, 0, 0, 0);
+      bool tok_ready = false;
+      int4 desc = first_desc<GROUPED>(p, first, n_items, NT);
+      for (int i = first; next_item<GROUPED>(p, i, stride, n_items, NT, KB, desc, it) && !*abort_flag;
+           i += stride) {
+        const Src src = item_src(it);
+        if (VARIANT & 2) {
+          // this item's token rows (loaded during the previous item, four per lane); rows past
+          // the tile's count repeat its last row (their accumulator columns are never stored),
+          // indices clamped into x (prep reports bad ones)
+          if (!tok_ready) tok_regs = load_tokens(it);
+          tok_idx[lane] = min(max(tok_regs.x, 0), p.T - 1);
+          tok_idx[lane + 32] = min(max(tok_regs.y, 0), p.T - 1);
+          tok_idx[lane + 64] = min(max(tok_regs.z, 0), p.T - 1);
+          tok_idx[lane + 96] = min(max(tok_regs.w, 0), p.T - 1);
+          __syncwarp();
+          Item nx;  // start the next item's index loads now; they land while this item streams
+          tok_ready = get_item<GROUPED>(p, i + stride, n_items, NT, KB, nx);
+          if (tok_ready) tok_regs = load_tokens(nx);
+        }
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
+          if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag, wd)) break;
+          if (!have_pol && issued >= STAGES && *policies_ready) {
+            __threadfence_block();
+            pol_x = policies[1];
+            have_pol = true;
+          }
+          ++issued;
+          if (elect_one()) issue_tokens(s, kb, src, have_pol, pol_x);
+          __syncwarp();
+          issued_phase[s] = ph;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      // Its copies in flight land before the CTA leaves (after an abort the stage's barrier
+      // may never complete: the wait is bounded).
+      for (int j = 0; j < STAGES; ++j)
+        if (issued_phase[j] >= 0) {
+          volatile int32_t dummy = 0;
+          mbar_wait_warp(&full[j], issued_phase[j], &dummy, wd);
+        }
+    }
   } else if (warp == kStreamWaiterWarp) {
     // Owns every wait in front of the MMA warp (the item's accumulator buffer being
     // free, then each stage's bytes) and hands the verdict over through bar.red, so
