@@ -108,13 +108,13 @@ DEVI int4 first_desc(const StreamArgs& p, int first, int n_items, int NT) {
   return (GROUPED && first < n_items) ? __ldg(p.tiles + first / NT) : make_int4(0, 0, 0, 0);
 }
 
-// Warp roles: 0 TMA producer (grouped: the weight part of each stage), 1 MMA issuer, 2-5
+// Warp roles: 0 weight producer (each stage's weight tile and scales), 1 MMA issuer, 2-5
 // epilogue, 6 stage waiter (waits for a stage's bytes and hands it to the MMA warp through
 // a named barrier, so that the MMA-issuing warp itself never waits on an mbarrier per
-// stage), 7 grouped: token producer.
+// stage), 7 token producer (each stage's token rows and scales).
 constexpr int kStreamThreads = 256;
 constexpr int kStreamWaiterWarp = 6;
-constexpr int kStreamTokenWarp = 7;  // grouped path: token rows and their scales
+constexpr int kStreamTokenWarp = 7;  // token rows and their scales
 constexpr uint32_t kStreamHandoffBarrier = 1;
 constexpr uint32_t kStreamEpilogueBarrier = 2;  // the 4 epilogue warps
 
@@ -201,19 +201,16 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
     else
       bulk_load_plain(st + L.sfx_off, src.sfx + kb * 2048, nsub * 512, bar);
   };
-  // Requests stage st_idx = K block kb of an item: the 128-row weight tile and its
-  // scales, and on the dense path, unless deferred (with_x false), the token tile and its
-  // scales (the grouped path's token warp requests those, issue_tokens).
-  auto issue_stage = [&](int st_idx, int kb, const Src& src, bool with_x, bool hint, uint64_t pol_w,
-                         uint64_t pol_x) {
-    const int n16 = src.n16;
+  // Weight warp: requests stage st_idx = K block kb of an item, the 128-row weight tile and
+  // its scales (and metadata), with their expected bytes on the stage's barrier, which
+  // counts two arrivals: this one and the token warp's (issue_tokens).
+  auto issue_stage = [&](int st_idx, int kb, const Src& src, bool hint, uint64_t pol_w) {
     const int32_t wrow0 = src.wrow0;
     const uint8_t* sfw = src.sfw;
     const int nsub = min(4, (K - kb * KSTAGE) / KMMA);
     uint8_t* st = smem + st_idx * L.stage_bytes;
     uint64_t* bar = &full[st_idx];
-    mbar_arrive_expect_tx(bar, 16384 + nsub * 512 + (SPARSE ? 4096 : 0) +
-                                   (GROUPED ? 0 : (SPARSE ? 2 : 1) * n16 * 2048 + nsub * 512));
+    mbar_arrive_expect_tx(bar, 16384 + nsub * 512 + (SPARSE ? 4096 : 0));
     if (hint) {
       tma_load_2d(st, &tmW, bar, kb * 128, wrow0, pol_w);
       bulk_load(st + L.sfw_off, sfw + kb * 2048, nsub * 512, bar, pol_w);
@@ -223,18 +220,16 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
       bulk_load_plain(st + L.sfw_off, sfw + kb * 2048, nsub * 512, bar);
       if (SPARSE) bulk_load_plain(st + L.meta_off, src.meta + kb * 4096, 4096, bar);
     }
-    if (!GROUPED && with_x) issue_x(st, bar, kb, src, hint, pol_x);
   };
-  // Grouped path, token warp: the token rows of stage st_idx (one tile load per 16 rows, or
-  // with a token gather four rows per tile::gather4 from the one-row-box map of x) and
-  // their scales, with their own expected bytes on the stage's barrier (which counts the
-  // weight warp's and the token warp's arrivals).
+  // Token warp: the token rows of stage st_idx (one tile load per 16 rows, or with a token
+  // gather four rows per tile::gather4 from the one-row-box map of x) and their scales,
+  // with their own expected bytes on the stage's barrier.
   auto issue_tokens = [&](int st_idx, int kb, const Src& src, bool hint, uint64_t pol_x) {
     const int nsub = min(4, (K - kb * KSTAGE) / KMMA);
     uint8_t* st = smem + st_idx * L.stage_bytes;
     uint64_t* bar = &full[st_idx];
     mbar_arrive_expect_tx(bar, (SPARSE ? 2 : 1) * src.n16 * 2048 + nsub * 512);
-    if (VARIANT & 2) {
+    if (GROUPED && (VARIANT & 2)) {
       for (int j = 0; j < src.n16 * 4; ++j)
         tma_gather4(st + L.x_off + j * 512, &tmX, bar, kb * 128, tok_idx[4 * j], tok_idx[4 * j + 1],
                     tok_idx[4 * j + 2], tok_idx[4 * j + 3]);
@@ -261,7 +256,7 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
     prefetch_tmap(&tmW);  // first, so that the descriptors are fetched while the barriers are set up
     prefetch_tmap(&tmX);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], GROUPED ? 2 : 1);  // grouped: the weight warp and the token warp arrive
+      mbar_init(&full[s], 2);  // the weight warp and the token warp arrive
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -296,7 +291,7 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
     if (p.pdl == 2) griddep_wait();  // set-up-only overlap: no load before the previous kernel completes
     for (int j = 0; j < n_pre; ++j)
       if (!(cta == 0 && j + 1 == p.drop_stage))  // test hook: stage withheld
-        issue_stage(j, first_it.kb0 + j, src, p.pdl != 1, p.w_keep != 0, keep, keep);
+        issue_stage(j, first_it.kb0 + j, src, p.w_keep != 0, keep);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, p.tmem_cols);
@@ -331,19 +326,16 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
   if (warp == 0) {
     // The first ring goes out without L2 hints; createpolicy costs ~0.6 us, so an idle
     // epilogue warp builds the policies and the producer picks them up once published.
-    uint64_t pol_w = 0, pol_x = 0;
+    uint64_t pol_w = 0;
     bool have_pol = false;
     int issued = 0;
     int s = 0;
     uint32_t ph = 0;
     int issued_phase[16];
     for (int i = 0; i < 16; ++i) issued_phase[i] = -1;
-    // Dense path under a programmatic dependency: the first ring of weight tiles is
-    // requested before waiting for the previous kernel; the token tiles (which that
-    // kernel may have produced) only after it.
-    bool pending = !GROUPED && p.pdl == 1;
+    // Under a programmatic dependency in the set-up-only form no weight is requested before
+    // the previous kernel completes; with NVFP4_TUNE_PDL = 1 the weights go out at once.
     if (p.pdl == 2) griddep_wait();
-    int pend_stage[16], pend_kb[16], npend = 0;
     Item it;
     int4 desc = first_desc<GROUPED>(p, first, n_items, NT);
     for (int i = first; next_item<GROUPED>(p, i, stride, n_items, NT, KB, desc, it) && !*abort_flag; i += stride) {
@@ -353,32 +345,17 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
         if (!have_pol && issued >= STAGES && *policies_ready) {
           __threadfence_block();
           pol_w = policies[0];
-          pol_x = policies[1];
           have_pol = true;
         }
         const bool pre = issued < n_pre;  // requested in the prologue
         ++issued;
         const bool withheld = cta == 0 && issued == p.drop_stage;  // test hook
-        if (!pre && !withheld && elect_one()) issue_stage(s, kb, src, !pending, have_pol, pol_w, pol_x);
+        if (!pre && !withheld && elect_one()) issue_stage(s, kb, src, have_pol, pol_w);
         __syncwarp();
-        if (pending) {
-          pend_stage[npend] = s;
-          pend_kb[npend] = kb;
-          ++npend;
-        }
         issued_phase[s] = ph;
         if (++s == STAGES) {
           s = 0;
           ph ^= 1;
-        }
-        if (pending && (npend == STAGES || kb + 1 == it.kb1)) {
-          griddep_wait();
-          if (elect_one()) {
-            for (int j = 0; j < npend; ++j)
-              issue_x(smem + pend_stage[j] * L.stage_bytes, &full[pend_stage[j]], pend_kb[j], src, false, 0);
-          }
-          __syncwarp();
-          pending = false;
         }
       }
     }
@@ -389,10 +366,14 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
         mbar_wait_warp(&full[i], issued_phase[i], &dummy, wd);
       }
   } else if (warp == kStreamTokenWarp) {
-    // Grouped path: requests every stage's token rows and their scales, in the weight warp's
-    // item and stage order (two warps issue a stage's copies in about half the time one
-    // does; with one, the issuing thread limited each CTA's weight stream). Dense path: idle.
-    if (GROUPED) {
+    // Requests every stage's token rows and their scales, in the weight warp's item and
+    // stage order (two warps issue a stage's copies in about half the time one does; with
+    // one, the issuing thread limited each CTA's weight stream, and on the decode path the
+    // first ring left ~1 us after the CTA started). The token rows and scales may come
+    // from the previous kernel in the stream: under a programmatic dependency this warp
+    // waits for it first.
+    if (p.pdl) griddep_wait();
+    {
       uint64_t pol_x = 0;
       bool have_pol = false;
       int issued = 0;
