@@ -797,6 +797,26 @@ def run_moe(m, synth, dev, stream, to_dev, quantize_dev, hbm, out):
                        "layer": "gate/up + SwiGLU, amax + quantise of the activation, down projection (one graph)",
                        "layer_weight_GBps": (mbytes + dbytes) / (ms_layer * 1e-3) / 1e9,
                        "layer_hbm_frac": (mbytes + dbytes) / (ms_layer * 1e-3) / 1e9 / hbm}
+
+    # The same layer with the gate/up epilogue emitting NVFP4 for the down projection, the
+    # activation's global scale given (calibrated once: the value the amax above produced).
+    def gate_up_nvfp4(i):
+        m.nvfp4_grouped_gemm_swiglu_quantize_out(qa, sfa, ga, qb, sfb, gb, off_d, E, Mt, N, K, g_a, q_out=q_a,
+                                                 sf_out=sf_a, workspace=wsp)
+
+    def layer_nvfp4(i):
+        gate_up_nvfp4(i)
+        down(i)
+
+    ms_guq = time_graph(gate_up_nvfp4, 4, 5, stream)
+    ms_layer_q = time_graph(layer_nvfp4, 2, 5, stream)
+    out["moe_layer_nvfp4_act"] = {
+        "gate_up_swiglu_nvfp4_us": ms_guq * 1e3,
+        "gate_up_swiglu_nvfp4_hbm_frac": mbytes / (ms_guq * 1e-3) / 1e9 / hbm,
+        "layer_us": ms_layer_q * 1e3,
+        "layer_weight_GBps": (mbytes + dbytes) / (ms_layer_q * 1e-3) / 1e9,
+        "layer_hbm_frac": (mbytes + dbytes) / (ms_layer_q * 1e-3) / 1e9 / hbm,
+        "layer": "gate/up + SwiGLU emitting NVFP4 (given activation scale), down projection (one graph)"}
     del y_act, qd, sd, y_dn
     a_s, off_s, _ = synth.moe_tokens(512, E, 8, K, 3, zipf_s=1.0)
     qs, sfs, gs = quantize_dev(to_dev(a_s))

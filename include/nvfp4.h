@@ -197,6 +197,30 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, const float*
                               size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * The same gate/up projection with SwiGLU, emitting NVFP4 for the down projection instead
+ * of bf16 ("The Moment of Synthesis", magik.net, Reasoning: the gate+up output feeds the
+ * K = 2048 down-projection grouped GEMM). The epilogue forms each output's bf16 value exactly
+ * as nvfp4_grouped_gemm_swiglu does and quantises it with the caller's global scale g_out
+ * (a calibrated activation scale: a tensor-wide amax cannot exist before the outputs do)
+ * by the recipe of nvfp4_quantize. So the codes and scales equal, bit for bit,
+ * nvfp4_quantize(nvfp4_grouped_gemm_swiglu(...), g_out).
+ *   g_out      device fp32 [1], decode-direction global scale of the output
+ *   q_out      device u8 [M_total, N_gu / 4], packed E2M1 codes
+ *   sf_out     device u8, nvfp4_scale_bytes(M_total, N_gu / 2) bytes, tiled E4M3 scales;
+ *              the padding rows up to a multiple of 128 are written 0
+ *   N_gu       a multiple of 128 (each epilogue warp then owns whole 16-element blocks)
+ * Other arguments as nvfp4_grouped_gemm_swiglu (no y). Returns
+ * NVFP4_ERR_UNSUPPORTED_SHAPE for N_gu not a multiple of 128, NVFP4_ERR_INVALID_ARG for a
+ * null q_out, sf_out or g_out, otherwise as nvfp4_grouped_gemm.
+ */
+int nvfp4_grouped_gemm_swiglu_quantize_out(const uint8_t* a, const uint8_t* sfa, const float* ga,
+                                           const uint8_t* b_gu, const uint8_t* sfb_gu, const float* gb,
+                                           const int32_t* expert_offsets, int32_t E, int64_t M_total, int64_t N_gu,
+                                           int64_t K, const float* g_out, uint8_t* q_out, uint8_t* sf_out,
+                                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                           void* stream);
+
+/*
  * Pair-wise 2:4 sparse NVFP4 ("FP4 structured sparsity", named as a kernel-level lever in
  * "The Moment of Recalibration", magik.net, The Broader Narrative Arc; the pages give no
  * format). The sparse block-scaled tensor-core MMA on FP4 keeps two of the four pairs of

@@ -46,7 +46,8 @@ EXPORTS = ["nvfp4_status_string", "nvfp4_scale_bytes", "nvfp4_amax_workspace_byt
            "nvfp4_encode_e2m1",
            "nvfp4_encode_e4m3", "nvfp4_tune", "nvfp4_last_launch_count",
            "nvfp4_sparse_meta_bytes", "nvfp4_scale_bytes_b32", "nvfp4_prune_pairs", "nvfp4_quantize_b32",
-           "nvfp4_sparse_gemm", "nvfp4_grouped_sparse_gemm", "nvfp4_gemm_batched"]
+           "nvfp4_sparse_gemm", "nvfp4_grouped_sparse_gemm", "nvfp4_gemm_batched",
+           "nvfp4_grouped_gemm_swiglu_quantize_out"]
 
 
 class NVFP4Error(RuntimeError):
@@ -121,6 +122,8 @@ def lib():
             L.nvfp4_grouped_sparse_gemm.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64,
                                                     _i64, _vp, _vp, _sz, _vp, _vp]
             L.nvfp4_gemm_batched.argtypes = [_vp, _i32, _i64, _vp, _vp]
+            L.nvfp4_grouped_gemm_swiglu_quantize_out.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64,
+                                                                 _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp, _vp]
             L.nvfp4_last_launch_count.restype = ctypes.c_int
             _lib = L
     return _lib
@@ -357,6 +360,30 @@ def nvfp4_quantize_b32(x: torch.Tensor, global_scale: torch.Tensor, q_out=None, 
               if sf_out is None else sf_out)
     _check("nvfp4_quantize_b32", lib().nvfp4_quantize_b32(_ptr(x), M, K, _ptr(global_scale), _ptr(q_out),
                                                           _ptr(sf_out), _stream(stream)))
+    return q_out, sf_out
+
+
+def nvfp4_grouped_gemm_swiglu_quantize_out(a, sfa, ga, b_gu, sfb_gu, gb, expert_offsets, E: int, M_total: int,
+                                           N_gu: int, K: int, g_out, q_out=None, sf_out=None, workspace=None,
+                                           dev_status=None, stream=None):
+    """Gate/up projection with SwiGLU emitting NVFP4 with the global scale g_out: returns
+    (codes u8 [M_total, N_gu // 4], tiled scales u8 [nvfp4_scale_bytes(M_total, N_gu // 2)])."""
+    for t, n in ((a, "a"), (sfa, "sfa"), (b_gu, "b_gu"), (sfb_gu, "sfb_gu")):
+        _cuda(t, torch.uint8, n)
+    for t, n in ((ga, "ga"), (gb, "gb"), (g_out, "g_out")):
+        _cuda(t, torch.float32, n)
+    dev = a.device
+    q_out = torch.empty((M_total, N_gu // 4), dtype=torch.uint8, device=dev) if q_out is None else q_out
+    sf_out = (torch.empty(nvfp4_scale_bytes(M_total, N_gu // 2), dtype=torch.uint8, device=dev)
+              if sf_out is None else sf_out)
+    ws_bytes = int(lib().nvfp4_grouped_gemm_workspace_bytes(E, M_total, N_gu, K))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    _check("nvfp4_grouped_gemm_swiglu_quantize_out",
+           lib().nvfp4_grouped_gemm_swiglu_quantize_out(_ptr(a), _ptr(sfa), _ptr(ga), _ptr(b_gu), _ptr(sfb_gu),
+                                                        _ptr(gb), _ptr(expert_offsets), E, M_total, N_gu, K,
+                                                        _ptr(g_out), _ptr(q_out), _ptr(sf_out), _ptr(workspace),
+                                                        workspace.numel(), _ptr(dev_status), _stream(stream)))
     return q_out, sf_out
 
 

@@ -717,7 +717,8 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
                         const float* gb, const int32_t* expert_offsets, int32_t E, int64_t M_total, int64_t N,
                         int64_t K, uint16_t* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                         void* stream, int swiglu, const int32_t* row_token = nullptr, int64_t T = 0,
-                        const uint8_t* meta = nullptr) {
+                        const uint8_t* meta = nullptr, uint8_t* q_out = nullptr, uint8_t* sf_out = nullptr,
+                        const float* g_out = nullptr) {
   g_last_launches = 0;
   const bool sparse = meta != nullptr;
   if (sparse && K % 128 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
@@ -730,8 +731,11 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   // preparation kernel's grid stride
   if (M_total > (int64_t(1) << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (M_total == 0) return NVFP4_OK;
-  if (!a || !sfa || !ga || !b || !sfb || !gb || !expert_offsets || !y) return NVFP4_ERR_INVALID_ARG;
-  if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(y))
+  const bool qout = q_out != nullptr;
+  if (!a || !sfa || !ga || !b || !sfb || !gb || !expert_offsets || (!qout && !y)) return NVFP4_ERR_INVALID_ARG;
+  if (qout && (!sf_out || !g_out)) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || (!qout && !aligned16(y)) ||
+      (qout && (!aligned16(q_out) || !aligned16(sf_out))))
     return NVFP4_ERR_ALIGNMENT;
   if (!workspace || workspace_bytes < nvfp4_grouped_gemm_workspace_bytes(E, M_total, N, K))
     return NVFP4_ERR_WORKSPACE;
@@ -740,6 +744,12 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   rc = device_info(d);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (qout && M_total % 128 != 0) {
+    // The scale tensor's padding rows (up to a multiple of 128) read as zero: the last
+    // 128-row group's scale tiles are cleared first, then the kernel writes its rows' bytes.
+    const int64_t kc4o = (N / 2) / 64;
+    if ((rc = from_cuda(cudaMemsetAsync(sf_out + (M_total / 128) * kc4o * 512, 0, kc4o * 512, st)))) return rc;
+  }
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* n_tiles = reinterpret_cast<int32_t*>(ws);
@@ -801,14 +811,17 @@ static int grouped_impl(const uint8_t* a, const uint8_t* sfa, const float* ga, c
   s.acc_cols = tile_rows;
   s.acc_bufs = 2;
   s.swiglu = swiglu;
+  s.q_out = q_out;
+  s.sf_out = sf_out;
+  s.g_out = g_out;
   const int sf_cols = sparse ? 40 : 32;  // TMEM columns per stage: scales (+ metadata)
   const int stage_bytes = stream_smem_bytes(1, s.x_rows, 0, sparse) - 1536;
   int stages = g_tune.grouped_stages;
-  if (stages == 0) stages = (kSmemLimit - 1536 - grouped_extra_bytes(tile_rows)) / stage_bytes;
+  if (stages == 0) stages = (kSmemLimit - 1536 - grouped_extra_bytes(tile_rows, qout)) / stage_bytes;
   const int tmem_room = (512 - 2 * s.acc_cols) / sf_cols;
   if (stages > tmem_room) stages = tmem_room;
   if (stages > 16) stages = 16;
-  if (stream_smem_bytes(stages, s.x_rows, grouped_extra_bytes(tile_rows), sparse) > kSmemLimit)
+  if (stream_smem_bytes(stages, s.x_rows, grouped_extra_bytes(tile_rows, qout), sparse) > kSmemLimit)
     return NVFP4_ERR_UNSUPPORTED_SHAPE;
   s.stages = stages;
   s.tmem_cols = pow2_at_least(2 * s.acc_cols + sf_cols * stages);
@@ -853,6 +866,19 @@ int nvfp4_grouped_gemm_swiglu(const uint8_t* a, const uint8_t* sfa, const float*
                               size_t workspace_bytes, int32_t* dev_status, void* stream) {
   return grouped_impl(a, sfa, ga, b_gu, sfb_gu, gb, expert_offsets, E, M_total, N_gu, K, y, workspace,
                       workspace_bytes, dev_status, stream, 1);
+}
+
+int nvfp4_grouped_gemm_swiglu_quantize_out(const uint8_t* a, const uint8_t* sfa, const float* ga,
+                                           const uint8_t* b_gu, const uint8_t* sfb_gu, const float* gb,
+                                           const int32_t* expert_offsets, int32_t E, int64_t M_total, int64_t N_gu,
+                                           int64_t K, const float* g_out, uint8_t* q_out, uint8_t* sf_out,
+                                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                           void* stream) {
+  g_last_launches = 0;
+  if (N_gu > 0 && N_gu % 128 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;  // whole 16-element output blocks per warp
+  if (M_total > 0 && !q_out) return NVFP4_ERR_INVALID_ARG;
+  return grouped_impl(a, sfa, ga, b_gu, sfb_gu, gb, expert_offsets, E, M_total, N_gu, K, nullptr, workspace,
+                      workspace_bytes, dev_status, stream, 1, nullptr, 0, nullptr, q_out, sf_out, g_out);
 }
 
 }  // extern "C"

@@ -20,6 +20,7 @@
 #include <stdint.h>
 
 #include "kernels.h"
+#include "nvfp4_quant.cuh"
 #include "ptx.cuh"
 
 namespace nvfp4 {
@@ -118,7 +119,8 @@ constexpr int kStreamTokenWarp = 7;  // token rows and their scales
 constexpr uint32_t kStreamHandoffBarrier = 1;
 constexpr uint32_t kStreamEpilogueBarrier = 2;  // the 4 epilogue warps
 
-// VARIANT: bit 0 SwiGLU epilogue, bit 1 token gather in the load stage (grouped only);
+// VARIANT: bit 0 SwiGLU epilogue (with bit 3: emitting NVFP4), bit 1 token gather in the load
+// stage (grouped only);
 // bit 2 pair-wise 2:4 sparse weights (dense or plain grouped path): the weight tile holds compressed
 // values, a stage spans 512 K elements (four K = 128 sparse MMAs) and carries the metadata
 // tile. Compiled separately so that the plain kernels carry none of them.
@@ -154,6 +156,9 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
   float* recv = reinterpret_cast<float*>(smem + STAGES * L.stage_bytes + 512);
   // grouped with a token gather: the x rows (token indices) of the producer's current item
   int32_t* tok_idx = reinterpret_cast<int32_t*>(smem + STAGES * L.stage_bytes + 512);
+  // grouped SwiGLU emitting NVFP4: one [32 tokens][16 columns] bf16 transpose tile per
+  // epilogue warp, after the token indices
+  uint16_t* xpose = reinterpret_cast<uint16_t*>(smem + STAGES * L.stage_bytes + 512 + grouped_extra_bytes(p.x_rows));
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -535,6 +540,8 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
     if (!GROUPED && p.pdl) griddep_wait();  // the global scales may come from the previous kernel
     const int q = warp & 3;
     const float ga = __ldg(p.ga);
+    const float gq = (VARIANT & 8) ? __ldg(p.g_out) : 1.0f;  // NVFP4 output: the caller's global scale
+    const float gq_inv = __frcp_rn(gq);
     const float gb0 = GROUPED ? 0.0f : __ldg(p.gb);  // dense: read while the mainloop runs
     dense_alpha = ga * gb0;
     int buf = 0;
@@ -556,7 +563,41 @@ DEVI void stream_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const Stre
           uint32_t r[32];
           tmem_ld32(tbase + c, r);
           tmem_ld_wait();
-          if (VARIANT & 1) {
+          if (VARIANT & 8) {
+            // SwiGLU emitting NVFP4. The even lanes' bf16 silu(gate) * up of this chunk's tokens
+            // go to the warp's transpose tile ([token][16 output columns]: this warp's 32 weight
+            // rows are 16 gate/up pairs, one whole 16-element block of every token row); then
+            // lane l quantises token c + l's block with the stand-alone quantiser's device code
+            // and the caller's global scale, so the codes equal nvfp4_quantize of the bf16
+            // output of the plain SwiGLU epilogue.
+            uint16_t* tt = xpose + q * 512;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (c + j < it.rows) {
+                const float v = __uint_as_float(r[j]) * alpha;
+                const float up = __shfl_xor_sync(0xffffffffu, v, 1);
+                if ((lane & 1) == 0) {
+                  const float act = v / (1.0f + __expf(-v));
+                  tt[j * 16 + (lane >> 1)] = __bfloat16_as_ushort(__float2bfloat16_rn(act * up));
+                }
+              }
+            __syncwarp();
+            if (c + lane < it.rows) {
+              const uint4 h0 = *reinterpret_cast<const uint4*>(tt + lane * 16);
+              const uint4 h1 = *reinterpret_cast<const uint4*>(tt + lane * 16 + 8);
+              const uint32_t w[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+              uint32_t sc;
+              uint2 pk;
+              quantize_block(w, gq, gq_inv, sc, pk);
+              const int64_t row = it.row0 + c + lane;
+              const int cb = it.wt * 4 + q;        // 16-column block of the N / 2 outputs
+              const int64_t kc4o = N >> 7;         // 512-byte scale tiles per 128 rows
+              *reinterpret_cast<uint2*>(p.q_out + row * (N >> 2) + cb * 8) = pk;
+              p.sf_out[((row >> 7) * kc4o + (cb >> 2)) * 512 + (row & 31) * 16 + ((row & 127) >> 5) * 4 + (cb & 3)] =
+                  static_cast<uint8_t>(sc);
+            }
+            __syncwarp();
+          } else if (VARIANT & 1) {
             // Weight rows 2c and 2c + 1 (gate and up of output column c) sit in adjacent
             // lanes: the even lane takes its partner's value and writes silu(gate) * up.
             const int n_out = N >> 1;
@@ -811,7 +852,9 @@ template <bool GROUPED, int VARIANT>
 static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tmX, const StreamArgs& a, int grid,
                                    cudaStream_t st) {
   // grouped: the token indices of a tile (the token gather); dense: the reduction's receive area
-  const int smem = stream_smem_bytes(a.stages, a.x_rows, GROUPED ? grouped_extra_bytes(a.x_rows) : stream_recv_bytes(a.M, a.split),
+  const int smem = stream_smem_bytes(a.stages, a.x_rows,
+                                     GROUPED ? grouped_extra_bytes(a.x_rows, (VARIANT & 8) != 0)
+                                             : stream_recv_bytes(a.M, a.split),
                                      (VARIANT & 4) != 0);
   cudaError_t e = allow_max_smem(reinterpret_cast<const void*>(k_gemm_stream<GROUPED, VARIANT>));
   if (e != cudaSuccess) return e;
@@ -843,8 +886,6 @@ static cudaError_t launch_stream_t(const CUtensorMap& tmW, const CUtensorMap& tm
 
 // Receive area of the one-way split-K reduction: S slots of ceil(M / S) tokens x 128 fp32.
 int stream_recv_bytes(int M, int split) { return split > 1 ? split * ((M + split - 1) / split) * 512 : 0; }
-
-int grouped_extra_bytes(int x_rows) { return x_rows * 4 > 256 ? x_rows * 4 : 256; }
 
 int stream_smem_bytes(int stages, int x_rows, int recv_bytes, bool sparse) {
   return stages * StreamLayout(x_rows, sparse).stage_bytes + recv_bytes + 1024 + 512;
@@ -885,6 +926,7 @@ cudaError_t launch_stream(const CUtensorMap& tmW, const CUtensorMap& tmX, const 
   if (a.row_token && a.swiglu) return cudaErrorInvalidValue;
   if (a.meta) return launch_stream_t<true, 4>(tmW, tmX, a, grid, st);
   if (a.row_token) return launch_stream_t<true, 2>(tmW, tmX, a, grid, st);
+  if (a.swiglu && a.q_out) return launch_stream_t<true, 9>(tmW, tmX, a, grid, st);
   if (a.swiglu) return launch_stream_t<true, 1>(tmW, tmX, a, grid, st);
   return launch_stream_t<true, 0>(tmW, tmX, a, grid, st);
 }

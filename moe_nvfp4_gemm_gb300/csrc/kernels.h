@@ -73,6 +73,11 @@ struct StreamArgs {
   const uint8_t* meta;       // pair-wise 2:4 sparse weights: tiled metadata (null: dense weights)
   int64_t meta_stride;       // grouped: bytes of metadata per expert
   int l2_prefetch;           // dense: K blocks of the CTA's weight slice prefetched into L2 at entry
+  // grouped SwiGLU emitting NVFP4: codes [M, N/4] and tiled scales of [M, N/2] with the
+  // caller's global scale g_out; y is not written
+  uint8_t* q_out;
+  uint8_t* sf_out;
+  const float* g_out;
 };
 
 
@@ -120,7 +125,11 @@ cudaError_t launch_grouped_prep(const int32_t* offsets, const int32_t* row_token
                                 int32_t* n_tiles, int4* tiles, uint8_t* slabs, int32_t* status, int grid,
                                 cudaStream_t st, const uint8_t* x_tok = nullptr, uint8_t* xg = nullptr);
 int stream_smem_bytes(int stages, int x_rows, int recv_bytes, bool sparse = false);
-int grouped_extra_bytes(int x_rows);  // shared memory for one tile's token indices
+// shared memory after the ring for one tile's token indices (and with qout the epilogue's
+// NVFP4 transpose tiles, 1 KB per epilogue warp)
+__host__ __device__ inline int grouped_extra_bytes(int x_rows, bool qout = false) {
+  return (x_rows * 4 > 256 ? x_rows * 4 : 256) + (qout ? 4 * 1024 : 0);
+}
 int stream_recv_bytes(int M, int split);
 
 // Raises `func`'s dynamic shared-memory limit to the opt-in maximum, once per

@@ -154,3 +154,12 @@ def test_gemm_batched_host_validation(lib):
     assert _batched(lib, [ok, m.GemmProblem(16, 16, 16, 16, 16, 16, 16, 256, 100)], 2, 4) == -2  # K % 64
     assert _batched(lib, [ok, m.GemmProblem(16, 16, 16, 0, 16, 16, 16, 256, 512)], 2, 4) == -1   # null b
     assert _batched(lib, [ok, m.GemmProblem(16, 16, 16, 24, 16, 16, 16, 256, 512)], 2, 4) == -3  # misaligned b
+
+
+def test_grouped_swiglu_quantize_out_host_validation(lib):
+    def call(N_gu, q=16, M=8):
+        return lib.nvfp4_grouped_gemm_swiglu_quantize_out(P(16), P(16), P(16), P(16), P(16), P(16), P(16), 2, M, N_gu,
+                                                          256, P(16), P(q), P(16), P(256), 1 << 20, None, None)
+    assert call(136) == -2           # N_gu not a multiple of 128
+    assert call(256, q=0) == -1      # no code output
+    assert call(256, M=0) == 0       # no routed rows: nothing to do

@@ -309,3 +309,75 @@ def test_grouped_gather_bad_token_index_reported(copy):
                                 workspace=_gather_ws(copy, g.E, 8, N, K))
     torch.cuda.synchronize()
     assert st.item() == -8
+
+
+def _swiglu_then_quantize(g, g_out):
+    """The unfused reference on the GPU: the plain SwiGLU epilogue's bf16 output, then the
+    stand-alone quantiser with the same global scale."""
+    y = g.run_swiglu()
+    q, sf = m.nvfp4_quantize(y, g_out)
+    torch.cuda.synchronize()
+    return y, q, sf
+
+
+def _fused(g, g_out, status=None):
+    M, N_gu = g.Mt, g.N
+    q = torch.full((M, N_gu // 4), 0xAB, dtype=torch.uint8, device=dev())
+    sf = torch.full((m.nvfp4_scale_bytes(M, N_gu // 2),), 0xAB, dtype=torch.uint8, device=dev())
+    m.nvfp4_grouped_gemm_swiglu_quantize_out(to_dev(g.qa), to_dev(g.sfa), scalar(g.ga), to_dev(g.qb), to_dev(g.sfb),
+                                             to_dev(g.gb), to_dev(g.off), g.E, g.Mt, g.N, g.K, g_out, q_out=q,
+                                             sf_out=sf, dev_status=status)
+    torch.cuda.synchronize()
+    return q, sf
+
+
+@pytest.mark.parametrize("tile_rows", [0, 64])
+@pytest.mark.parametrize("counts,N_gu,K", [
+    ((3, 0, 17, 1, 0, 9), 256, 512),           # ragged, empty experts, 30 rows (scale padding rows)
+    ((64, 65, 1, 127, 0, 200), 384, 1088),     # tile boundaries, several 32-token chunks
+    ((0, 300, 0), 128, 256),                   # one expert, several token tiles, one weight tile
+])
+def test_grouped_swiglu_quantize_out_equals_quantised_swiglu(counts, N_gu, K, tile_rows):
+    # Codes and tiled scales (padding rows included, from garbage-filled outputs) equal the
+    # stand-alone quantiser applied to the plain SwiGLU epilogue's bf16 output, bit for bit;
+    # those codes also equal the oracle's quantiser on the same bf16 values, and the bf16
+    # values are within the SwiGLU tolerance of the oracle.
+    m.nvfp4_tune(m.NVFP4_TUNE_GROUPED_TILE_ROWS, tile_rows)
+    g = Grouped(counts, N_gu, K, 33)
+    y0 = g.run_swiglu()
+    _, g_out = m.nvfp4_amax(y0)
+    y, q_ref, sf_ref = _swiglu_then_quantize(g, g_out)
+    q, sf = _fused(g, g_out)
+    assert torch.equal(q, q_ref)
+    assert torch.equal(sf, sf_ref)
+    yb = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    qo, sfo, _ = oracle.quantize(yb, float(g_out.item()))
+    assert np.array_equal(q.cpu().numpy(), qo) and np.array_equal(sf.cpu().numpy(), sfo)
+    g.check_swiglu(y)
+
+
+def test_grouped_swiglu_quantize_out_moe_workload():
+    # gate+up of the MoE workload (256 experts, 512 tokens top-8, K = 6144, N_gu = 4096),
+    # every output row: fused codes and scales against the unfused path on the GPU
+    a_rows, off, tok = synth.moe_tokens(512, 256, 8, 6144, 3)
+    g = Grouped(tuple(np.diff(off)), 4096, 6144, 3, a_rows=a_rows,
+                w=lambda e: synth.moe_expert_weight(e, 4096, 6144, 3))
+    y0 = g.run_swiglu()
+    _, g_out = m.nvfp4_amax(y0)
+    _, q_ref, sf_ref = _swiglu_then_quantize(g, g_out)
+    q, sf = _fused(g, g_out)
+    assert torch.equal(q, q_ref)
+    assert torch.equal(sf, sf_ref)
+
+
+def test_grouped_swiglu_quantize_out_rejects_and_reports():
+    g = Grouped((4, 4), 256, 256, 34)
+    g_out = torch.ones(1, dtype=torch.float32, device=dev())
+    bad = Grouped((4, 4), 136, 256, 34)  # N_gu not a multiple of 128
+    with pytest.raises(m.NVFP4Error) as e:
+        _fused(bad, g_out)
+    assert e.value.status == -2
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    g.off = np.array([0, 5, 4], dtype=np.int32)  # decreasing offsets
+    _fused(g, g_out, status=st)
+    assert st.item() == -8
