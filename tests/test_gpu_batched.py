@@ -94,3 +94,45 @@ def test_batched_decode_workload_sampled():
     cols = np.unique(np.concatenate([np.arange(0, SQ, 128), np.arange(127, SQ, 128)]))
     for (A, B), y in zip(probs, _run(M, probs)):
         check_gemm(y, A, B, cols=cols)
+
+
+@pytest.mark.parametrize("pdl", [1, 2, -1])
+def test_batched_launches_keep_stream_order(pdl):
+    # Back-to-back batched launches inside one CUDA graph (1: weights requested before the
+    # launch dependency, 2: set-up overlap only, the default; -1: plain stream order),
+    # alternating between two sets of problems that all write the same outputs: every
+    # output write is ordered after the previous launch's, so the last launch's results win,
+    # and a launch writing its own outputs gets exactly its own results.
+    M = 16
+    p1 = _problems(M, [(256, 1024), (384, 512)], 600)
+    p2 = _problems(M, [(256, 1024), (384, 512)], 700)
+    m.nvfp4_tune(m.NVFP4_TUNE_PDL, -1)
+    r1 = [y.clone() for y in _run(M, p1)]
+    r2 = [y.clone() for y in _run(M, p2)]
+    m.nvfp4_tune(m.NVFP4_TUNE_PDL, pdl)
+    shared = [torch.empty_like(r) for r in r1]
+    own = [[torch.empty_like(r) for r in r1] for _ in range(5)]
+
+    def launch(probs, ys):
+        m.nvfp4_gemm_batched([(A.dq, A.dsf, A.dg, B.dq, B.dsf, B.dg, y) for (A, B), y in zip(probs, ys)], M)
+
+    sets = [p1, p2, p1, p2, p1]
+    for probs in sets[:2]:  # warm up outside capture
+        launch(probs, shared)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for probs, ys in zip(sets, own):
+            launch(probs, ys)
+        for probs in sets:
+            launch(probs, shared)
+    for y in shared:
+        y.fill_(0)
+    g.replay()
+    torch.cuda.synchronize()
+    for i, ys in enumerate(own):
+        ref = r1 if i % 2 == 0 else r2
+        for y, r in zip(ys, ref):
+            assert torch.equal(y.view(torch.int16), r.view(torch.int16)), i
+    for y, r in zip(shared, r1):
+        assert torch.equal(y.view(torch.int16), r.view(torch.int16))
