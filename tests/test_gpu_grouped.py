@@ -381,3 +381,15 @@ def test_grouped_swiglu_quantize_out_rejects_and_reports():
     g.off = np.array([0, 5, 4], dtype=np.int32)  # decreasing offsets
     _fused(g, g_out, status=st)
     assert st.item() == -8
+
+
+@pytest.mark.parametrize("g_value", [1e-30, 3e-36, 1e30])
+def test_grouped_swiglu_quantize_out_extreme_global_scales(g_value):
+    # global scales at and beyond the fast division's guard (the quantiser's IEEE-division
+    # fallback, saturating and all-zero codes): still nvfp4_quantize of the SwiGLU output
+    g = Grouped((7, 0, 40, 130), 256, 512, 35)
+    g_out = torch.tensor([g_value], dtype=torch.float32, device=dev())
+    _, q_ref, sf_ref = _swiglu_then_quantize(g, g_out)
+    q, sf = _fused(g, g_out)
+    assert torch.equal(q, q_ref)
+    assert torch.equal(sf, sf_ref)
