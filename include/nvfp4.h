@@ -330,8 +330,8 @@ int nvfp4_grouped_gemm_noalloc(const uint8_t* a, const uint8_t* sfa, const float
  * sharing M (1..128, the decode range: the weight-streaming kernel) but with its own
  * operands, N and K. One launch streams all the weights, so the fixed costs of a decode
  * call (launch, first-load latency, split-K reduction, tail) are paid once and overlap
- * other problems' streaming, instead of once per GEMM ("The Moment of Recalibration", The
- * Immediate Reckoning: small-M GEMMs far below the part's rates). Each problem's outputs are
+ * other problems' streaming, instead of once per GEMM ("The Moment of Recalibration", Input
+ * Knowledge Required: decode-size GEMMs far below the part's rates). Each problem's outputs are
  * within the GEMM tolerance of the oracle; the split-K cluster size is chosen for the whole
  * launch, so a problem's result may differ in the last bf16 place from a single
  * nvfp4_gemm call of it (bit for bit equal when both use the same split).
