@@ -13,9 +13,14 @@
 // stream reads each weight tile once; the tokens come from L2.
 //   dense decode: grid = (N/128) x S CTAs in clusters of S along K; each CTA
 //     reduces its K slice in TMEM, the S partials are summed through DSMEM.
+//   batched decode (k_gemm_batched): the dense decode body over a list of independent
+//     GEMMs in one launch, each problem's CTAs as a single call's grid would be.
 //   grouped: a persistent grid walks (token tile, weight tile) items built by
 //     k_grouped_prep (ragged per-expert counts, empty experts skipped); each
-//     item streams one expert's 128-row weight tile over all of K.
+//     item streams one expert's 128-row weight tile over all of K. Epilogues: bf16,
+//     SwiGLU (bf16, or NVFP4 with the caller's global scale).
+// Two warps issue each stage's copies (weight tile + scales; token rows + scales), each
+// with its own expected bytes on the stage's barrier.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
